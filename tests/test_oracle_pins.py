@@ -1,0 +1,457 @@
+"""Pins of the fp64 oracle to facts other than itself (CPU only).
+
+Each pin is chosen so that a plausible slip in the oracle (a dropped term, a
+wrong sign or index, a transposed operand, the wrong variance or GELU form)
+fails at least one of them: closed forms, library routines on special cases,
+exact rational arithmetic and brute force loops on tiny inputs.
+``test_oracle_mutations.py`` plants such slips and checks they are caught.
+"""
+import math
+from fractions import Fraction
+
+import mpmath
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from audio_diffusion_transformer_fwd_b300 import synth
+
+# ------------------------------------------------------------------ bf16 rounding
+
+
+def test_bf16_round_ties_and_library():
+    one = 1.0
+    ulp = 2.0 ** -7                        # BF16 spacing in [1, 2)
+    assert O.bf16_round(one + ulp / 2) == one                    # tie -> even (1.0)
+    assert O.bf16_round(one + 3 * ulp / 2) == one + 2 * ulp      # tie -> even
+    assert O.bf16_round(one + ulp / 2 + 2.0 ** -20) == one + ulp  # above the tie
+    r = np.random.default_rng(3).standard_normal(10000) * 37.0
+    ref = torch.from_numpy(r.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(O.bf16_round(r.astype(np.float32)), ref)
+
+
+# ------------------------------------------------------------------ LayerNorm / AdaLN
+
+
+def test_layer_norm_hand_example():
+    # mean 2.5, biased variance 1.25 (the unbiased one would be 5/3)
+    x = np.array([[1.0, 2.0, 3.0, 4.0]])
+    eps = 1e-6
+    want = (x - 2.5) / math.sqrt(1.25 + eps)
+    assert np.allclose(O.layer_norm(x, eps), want, rtol=0, atol=1e-15)
+
+
+def test_layer_norm_matches_torch():
+    x = np.random.default_rng(0).standard_normal((7, 96)) * 3 + 1.5
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(x), (96,), eps=1e-6).numpy()
+    assert np.allclose(O.layer_norm(x, 1e-6), ref, rtol=0, atol=1e-12)
+
+
+def test_adaln_special_cases():
+    r = np.random.default_rng(1)
+    x = r.standard_normal((5, 64))
+    shift = r.standard_normal(64)
+    # scale = -1 cancels the normalised row: the output is the shift exactly
+    assert np.allclose(O.adaln(x, shift, -np.ones(64), 1e-6), np.broadcast_to(shift, (5, 64)), atol=1e-15)
+    # zero shift and zero scale: plain LayerNorm, mean 0 and variance 1 - O(eps)
+    y = O.adaln(x, np.zeros(64), np.zeros(64), 1e-6)
+    assert np.allclose(y.mean(axis=1), 0, atol=1e-13)
+    assert np.allclose((y ** 2).mean(axis=1), 1, atol=1e-5)
+    # scale = 1 doubles it
+    assert np.allclose(O.adaln(x, np.zeros(64), np.ones(64), 1e-6), 2 * y, atol=1e-13)
+
+
+# ------------------------------------------------------------------ RoPE
+
+CFG_R = O.BlockConfig(d=256, heads=2, head_dim=128, ffn=64, rope_sections=(32, 48, 48))
+
+
+def test_rope_identity_at_origin_and_norm():
+    r = np.random.default_rng(2)
+    t = r.standard_normal((9, 2, 128))
+    assert np.allclose(O.apply_rope(t, np.zeros((9, 3)), CFG_R), t, atol=0)
+    pos = r.uniform(-50, 300, (9, 3))
+    rt = O.apply_rope(t, pos, CFG_R)
+    assert np.allclose(np.linalg.norm(rt, axis=-1), np.linalg.norm(t, axis=-1), rtol=1e-13)
+
+
+def test_rope_relative_position():
+    r = np.random.default_rng(4)
+    q = r.standard_normal((1, 1, 128))
+    k = r.standard_normal((1, 1, 128))
+    pm = r.uniform(0, 40, (1, 3))
+    pn = r.uniform(0, 40, (1, 3))
+    dots = []
+    for shift in ([0, 0, 0], [3.5, -7.0, 11.25], [100.0, 2.0, -30.0]):
+        a = O.apply_rope(q, pm + shift, CFG_R)
+        b = O.apply_rope(k, pn + shift, CFG_R)
+        dots.append(float((a * b).sum()))
+    assert np.allclose(dots, dots[0], rtol=1e-12)
+
+
+def test_rope_sections_axes_and_frequencies():
+    # a unit vector on pair i of each section turns by exactly pos_axis * theta^(-2i/sec)
+    sec = (32, 48, 48)
+    starts = (0, 32, 80)
+    theta = mpmath.mpf(10000)
+    for axis in range(3):
+        for i in (0, 1, 5, sec[axis] // 2 - 1):
+            dim = starts[axis] + 2 * i
+            t = np.zeros((1, 1, 128))
+            t[0, 0, dim] = 1.0
+            pos = np.zeros((1, 3))
+            pos[0, axis] = 17.0
+            out = O.apply_rope(t, pos, CFG_R)
+            ang = 17 * theta ** (mpmath.mpf(-2 * i) / sec[axis])
+            assert abs(out[0, 0, dim] - float(mpmath.cos(ang))) < 1e-13
+            assert abs(out[0, 0, dim + 1] - float(mpmath.sin(ang))) < 1e-13
+            # only that pair moves; a position on another axis leaves it alone
+            rest = np.delete(out[0, 0], [dim, dim + 1])
+            assert np.all(rest == 0)
+            pos2 = np.zeros((1, 3))
+            pos2[0, (axis + 1) % 3] = 17.0
+            assert np.allclose(O.apply_rope(t, pos2, CFG_R), t, atol=0)
+
+
+# ------------------------------------------------------------------ attention
+
+
+def _attention_loops(q, k, v):
+    h_, n, dh = q.shape
+    out = np.zeros((h_, n, v.shape[2]))
+    for h in range(h_):
+        for i in range(n):
+            s = [sum(q[h, i, c] * k[h, j, c] for c in range(dh)) / math.sqrt(dh) for j in range(n)]
+            mx = max(s)
+            e = [math.exp(x - mx) for x in s]
+            tot = sum(e)
+            for j in range(n):
+                out[h, i] += e[j] / tot * v[h, j]
+    return out
+
+
+def test_attention_brute_force_and_sdpa():
+    r = np.random.default_rng(5)
+    q, k, v = (r.standard_normal((2, 6, 4)) * 2 for _ in range(3))
+    assert np.allclose(O.attention(q, k, v), _attention_loops(q, k, v), atol=1e-13)
+    q, k, v = (r.standard_normal((3, 50, 16)) for _ in range(3))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q), torch.from_numpy(k), torch.from_numpy(v)).numpy()
+    assert np.allclose(O.attention(q, k, v), ref, atol=1e-12)
+    sub = O.attention(q, k, v, rows=[3, 17, 49])
+    assert np.allclose(sub, O.attention(q, k, v)[:, [3, 17, 49]], atol=0)
+
+
+def test_attention_identical_keys_is_mean_of_values():
+    r = np.random.default_rng(6)
+    q = r.standard_normal((2, 9, 8))
+    k = np.broadcast_to(r.standard_normal((2, 1, 8)), (2, 9, 8))
+    v = r.standard_normal((2, 9, 8))
+    assert np.allclose(O.attention(q, k, v), np.broadcast_to(v.mean(axis=1, keepdims=True), v.shape), atol=1e-14)
+
+
+def test_attention_one_token_returns_its_value():
+    r = np.random.default_rng(7)
+    q, k, v = (r.standard_normal((3, 1, 8)) for _ in range(3))
+    assert np.allclose(O.attention(q, k, v), v, atol=1e-15)
+
+
+# ------------------------------------------------------------------ GELU
+
+
+def test_gelu_tanh_closed_form():
+    x = np.array([-3.0, -1.0, -0.25, 0.0, 0.5, 1.0, 2.0, 6.0])
+    got = O.gelu_tanh(x)
+    c = mpmath.sqrt(2 / mpmath.pi)
+    for xi, gi in zip(x, got):
+        xm = mpmath.mpf(xi)
+        want = xm / 2 * (1 + mpmath.tanh(c * (xm + mpmath.mpf("0.044715") * xm ** 3)))
+        assert abs(gi - float(want)) < 1e-15
+    # odd part: GELU(x) - GELU(-x) = x
+    assert np.allclose(got - O.gelu_tanh(-x), x, atol=1e-15)
+    # within the tanh form's error of the erf form
+    erf_form = np.array([float(mpmath.mpf(xi) / 2 * (1 + mpmath.erf(mpmath.mpf(xi) / mpmath.sqrt(2)))) for xi in x])
+    assert np.max(np.abs(got - erf_form)) < 1e-3
+
+
+# ------------------------------------------------------------------ the block, brute force
+
+TINY = O.BlockConfig(d=12, heads=2, head_dim=6, ffn=20, eps=1e-6, rope_sections=(2, 2, 2))
+
+
+def _tiny_inputs(seed, n=5, gate_std=0.5):
+    r = np.random.default_rng(seed)
+    d, f = TINY.d, TINY.ffn
+    w = {"w_qkv": r.standard_normal((3 * d, d)) * 0.3, "w_o": r.standard_normal((d, d)) * 0.3,
+         "w1": r.standard_normal((f, d)) * 0.3, "w2": r.standard_normal((d, f)) * 0.3}
+    mod = r.standard_normal((6, d)) * gate_std
+    x = r.standard_normal((n, d))
+    pos = r.uniform(0, 9, (n, 3))
+    return x, w, mod, pos
+
+
+def _block_loops(x, w, mod, pos, cfg):
+    """The block written out element by element, independently of the numpy
+    formulation: every index of every contraction is explicit."""
+    n, d = x.shape
+    H, Dh, F = cfg.heads, cfg.head_dim, cfg.ffn
+    sh1, sc1, g1, sh2, sc2, g2 = mod
+
+    def ln_row(row, shift, scale):
+        mu = sum(row) / d
+        var = sum((a - mu) ** 2 for a in row) / d
+        return [(row[c] - mu) / math.sqrt(var + cfg.eps) * (1 + scale[c]) + shift[c] for c in range(d)]
+
+    def rot(vec, p):
+        out = list(vec)
+        start = 0
+        for axis, sec in enumerate(cfg.rope_sections):
+            for i in range(sec // 2):
+                ang = p[axis] * cfg.rope_theta ** (-2.0 * i / sec)
+                a, b = vec[start + 2 * i], vec[start + 2 * i + 1]
+                out[start + 2 * i] = a * math.cos(ang) - b * math.sin(ang)
+                out[start + 2 * i + 1] = a * math.sin(ang) + b * math.cos(ang)
+            start += sec
+        return out
+
+    h = [ln_row(x[t], sh1, sc1) for t in range(n)]
+    qkv = [[sum(h[t][c] * w["w_qkv"][o][c] for c in range(d)) for o in range(3 * d)] for t in range(n)]
+    Q = [[rot(qkv[t][hd * Dh:(hd + 1) * Dh], pos[t]) for t in range(n)] for hd in range(H)]
+    K = [[rot(qkv[t][d + hd * Dh:d + (hd + 1) * Dh], pos[t]) for t in range(n)] for hd in range(H)]
+    V = [[qkv[t][2 * d + hd * Dh:2 * d + (hd + 1) * Dh] for t in range(n)] for hd in range(H)]
+    o = [[0.0] * d for _ in range(n)]
+    for hd in range(H):
+        for i in range(n):
+            s = [sum(Q[hd][i][c] * K[hd][j][c] for c in range(Dh)) / math.sqrt(Dh) for j in range(n)]
+            mx = max(s)
+            e = [math.exp(z - mx) for z in s]
+            tot = sum(e)
+            for c in range(Dh):
+                o[i][hd * Dh + c] = sum(e[j] / tot * V[hd][j][c] for j in range(n))
+    x2 = []
+    for t in range(n):
+        a = [sum(o[t][c] * w["w_o"][oc][c] for c in range(d)) for oc in range(d)]
+        x1 = [x[t][c] + g1[c] * a[c] for c in range(d)]
+        h2 = ln_row(x1, sh2, sc2)
+        pre = [sum(h2[c] * w["w1"][j][c] for c in range(d)) for j in range(F)]
+        u = [0.5 * z * (1 + math.tanh(math.sqrt(2 / math.pi) * (z + 0.044715 * z ** 3))) for z in pre]
+        m = [sum(u[j] * w["w2"][c][j] for j in range(F)) for c in range(d)]
+        x2.append([x1[c] + g2[c] * m[c] for c in range(d)])
+    return np.array(x2)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_block_brute_force_tiny(seed):
+    x, w, mod, pos = _tiny_inputs(seed)
+    assert np.allclose(O.block_forward(x, w, mod, pos, TINY), _block_loops(x, w, mod, pos, TINY), atol=1e-12)
+
+
+def test_block_gate_zero_is_identity_and_rows():
+    x, w, mod, pos = _tiny_inputs(3)
+    mod0 = mod.copy()
+    mod0[2] = 0
+    mod0[5] = 0
+    assert np.array_equal(O.block_forward(x, w, mod0, pos, TINY), x)
+    full = O.block_forward(x, w, mod, pos, TINY)
+    assert np.allclose(O.block_forward(x, w, mod, pos, TINY, rows=[1, 4]), full[[1, 4]], atol=1e-14)
+
+
+def test_block_bf16_storage_is_close_and_rounded():
+    x, w, mod, pos = _tiny_inputs(4)
+    a = O.block_forward(x, w, mod, pos, TINY)
+    b = O.block_forward(x, w, mod, pos, TINY, bf16_storage=True)
+    assert np.array_equal(b, O.bf16_round(b))
+    assert np.linalg.norm(a - b) / np.linalg.norm(a) < 2e-2
+
+
+def test_block_flops_formula():
+    cfg = O.BlockConfig(d=5120, heads=40, head_dim=128, ffn=20480)
+    # the four projections 2*N*d*(3d + d + 2F) and attention 4*N^2*d
+    assert O.block_flops(6912, cfg) == pytest.approx(5.3270e12, rel=1e-4)
+    assert O.block_flops(10488, cfg) == pytest.approx(8.8512e12, rel=1e-4)
+
+
+# ------------------------------------------------------------------ quantisation
+
+
+def test_quantize_rows_exact_rational():
+    r = np.random.default_rng(8)
+    x = (r.standard_normal((6, 64)) * r.uniform(0.01, 30, (6, 1))).astype(np.float32)
+    x[2] = 0.0
+    q, s = O.quantize_rows(x)
+    assert q.dtype == np.int8 and s.dtype == np.float32
+    assert np.all(np.abs(q.astype(int)) <= 127)
+    assert np.all(q[2] == 0) and s[2, 0] == 0
+    for i in range(6):
+        if s[i, 0] == 0:
+            continue
+        # s is absmax / 127 rounded to binary32
+        assert abs(Fraction(float(s[i, 0])) - Fraction(float(np.abs(x[i]).max())) / 127) <= Fraction(float(s[i, 0])) * Fraction(1, 2 ** 24)
+        assert abs(int(q[i, np.argmax(np.abs(x[i]))])) == 127
+        for j in range(64):
+            exact = Fraction(float(x[i, j])) / Fraction(float(s[i, 0]))
+            nearest = round(exact)                       # Python rounds half to even
+            if abs(abs(exact - math.floor(exact)) - Fraction(1, 2)) > Fraction(1, 10 ** 5):
+                assert int(q[i, j]) == max(-127, min(127, nearest))
+            # reconstruction error at most half a step (plus the binary32 rounding of x / s)
+            assert abs(float(x[i, j]) - float(s[i, 0]) * int(q[i, j])) <= float(s[i, 0]) * (0.5 + 1e-5)
+
+
+def test_quantize_ties_to_even():
+    # absmax 127 gives the scale 1 exactly, so x / s = x and the halves are exact ties
+    x = np.array([[127.0, 2.5, 3.5, -2.5, -0.5, 0.5, 1.5, 126.5, -126.5]], np.float32)
+    q, s = O.quantize_rows(x)
+    assert s[0, 0] == 1.0
+    assert q.tolist() == [[127, 2, 4, -2, 0, 0, 2, 126, -126]]
+
+
+def test_quantize_groups_and_idempotence():
+    r = np.random.default_rng(9)
+    x = r.standard_normal((4, 3 * 32)).astype(np.float32)
+    q, s = O.quantize_rows(x, 32)
+    assert s.shape == (4, 3)
+    for g in range(3):
+        qg, sg = O.quantize_rows(x[:, g * 32:(g + 1) * 32])
+        assert np.array_equal(qg, q[:, g * 32:(g + 1) * 32]) and np.array_equal(sg[:, 0], s[:, g])
+    deq = (q.astype(np.float32).reshape(4, 3, 32) * s[:, :, None]).reshape(4, 96)
+    q2, _ = O.quantize_rows(deq, 32)
+    assert np.array_equal(q2, q)
+
+
+def test_gemm_int_and_fc2_groups_brute_force():
+    r = np.random.default_rng(10)
+    a = r.integers(-127, 128, (3, 8)).astype(np.int8)
+    b = r.integers(-127, 128, (5, 8)).astype(np.int8)
+    acc = O.gemm_int(a, b)
+    for i in range(3):
+        for j in range(5):
+            assert acc[i, j] == sum(int(a[i, k]) * int(b[j, k]) for k in range(8))
+    # worst case magnitudes stay exact (127*127*K)
+    big = np.full((1, 4096), 127, np.int8)
+    assert O.gemm_int(big, -big)[0, 0] == -127 * 127 * 4096
+    us = r.uniform(0.1, 2, (3, 2))
+    ws = r.uniform(0.1, 2, 5)
+    m = O.fc2_int8(a, us, b, ws, group=4)
+    for i in range(3):
+        for j in range(5):
+            want = ws[j] * sum(us[i, g] * sum(int(a[i, k]) * int(b[j, k]) for k in range(4 * g, 4 * g + 4))
+                               for g in range(2))
+            assert abs(m[i, j] - want) < 1e-9
+    # one group spanning all channels equals the plain dequantised projection
+    assert np.allclose(O.fc2_int8(a, us[:, :1], b, ws, group=8), O.linear_int8(a, us[:, 0], b, ws))
+
+
+# ------------------------------------------------------------------ token reduction
+
+
+def test_token_counts_of_the_workloads():
+    lines = [l.split() for l in open(__file__.replace("test_oracle_pins.py", "golden/token_counts.txt"))
+             if l.strip() and not l.startswith("#")]
+    for name, T, Hh, W, n_text, n_audio, n, n_red in lines:
+        T, Hh, W, n_text, n_audio, n, n_red = map(int, (T, Hh, W, n_text, n_audio, n, n_red))
+        assert T * Hh * W + n_text + n_audio == n
+        g = O.VideoGrid(0, T, Hh, W)
+        assert O.reduced_token_count(n, g) == n_red
+        assert synth.positions((T, Hh, W), n_text, n_audio).shape == (n, 3)
+
+
+def test_reduce_restore_identity_and_pairs():
+    r = np.random.default_rng(11)
+    g = O.VideoGrid(offset=3, T=2, Hh=3, W=5)        # odd W: last column unpaired
+    n = 3 + 30 + 4
+    x = O.bf16_round(r.standard_normal((n, 8)))
+    red, side = O.token_reduce(x, g, bf16_storage=True)
+    assert red.shape[0] == O.reduced_token_count(n, g) == n - 2 * 3 * 2
+    # text before and audio after pass through; a pair is the mean of its columns
+    assert np.array_equal(red[:3], x[:3]) and np.array_equal(red[-4:], x[-4:])
+    assert np.array_equal(red[3], O.bf16_round((x[3] + x[4]) / 2))
+    assert np.array_equal(red[5], x[7])               # (t=0, y=0) row: column 4 unpaired
+    # reduce then restore with a zero update is the identity, bit for bit
+    for storage in (False, True):
+        red, side = O.token_reduce(x, g, bf16_storage=storage)
+        assert np.array_equal(O.token_restore(red, side, g, bf16_storage=storage), x)
+    # a uniform update moves every member of every pair by that amount
+    red, side = O.token_reduce(x, g)
+    back = O.token_restore(red + 0.25, side, g)
+    assert np.allclose(back, x + 0.25, atol=1e-15)
+    # constant pairs reduce exactly
+    xc = np.repeat(r.standard_normal((n // 2 + 1, 8)), 2, axis=0)[:n]
+    gc = O.VideoGrid(offset=0, T=1, Hh=2, W=4)
+    redc, _ = O.token_reduce(xc[:8], gc)
+    assert np.array_equal(redc, xc[0:8:2])
+
+
+def test_reduced_positions_pair_mean():
+    g = O.VideoGrid(0, 2, 2, 4)
+    pos = synth.positions((2, 2, 4), 3, 2).astype(np.float64)
+    pr = O.reduced_positions(pos, g)
+    assert pr.shape == (8 + 5, 3)
+    assert np.array_equal(pr[0], [0, 0, 0.5]) and np.array_equal(pr[1], [0, 0, 2.5])
+    assert np.array_equal(pr[7], [1, 1, 2.5])
+    assert np.array_equal(pr[8:], pos[16:])
+
+
+# ------------------------------------------------------------------ the step
+
+
+def test_step_one_block_equals_block_and_zero_gates():
+    x, w, mod, pos = _tiny_inputs(12, n=6)
+    assert np.array_equal(O.step_forward(x, [w], [mod], pos, TINY), O.block_forward(x, w, mod, pos, TINY))
+    mods = []
+    for b in range(4):
+        m = mod.copy() * (b + 1)
+        m[2] = 0
+        m[5] = 0
+        mods.append(m)
+    assert np.array_equal(O.step_forward(x, [w] * 4, mods, pos, TINY), x)
+
+
+def test_step_with_reduction_boundaries():
+    cfg = TINY
+    r = np.random.default_rng(13)
+    g = O.VideoGrid(0, 1, 2, 4)
+    n = 8 + 3
+    x = r.standard_normal((n, cfg.d))
+    pos = synth.positions((1, 2, 4), 3, 0).astype(np.float64)
+    _, w, mod, _ = _tiny_inputs(14, n=n)
+    red = O.Reduction(grid=g, reduce_after_block=0, restore_before_block=2)
+    # zero gates: reduce + restore around identity blocks is the identity
+    m0 = mod.copy()
+    m0[2] = 0
+    m0[5] = 0
+    assert np.allclose(O.step_forward(x, [w] * 3, [m0] * 3, pos, cfg, reduction=red), x, atol=1e-15)
+    # by hand: block 0 full, block 1 reduced, restore, block 2 full
+    y0 = O.block_forward(x, w, mod, pos, cfg)
+    yr, side = O.token_reduce(y0, g)
+    y1 = O.block_forward(yr, w, mod * 0.5, O.reduced_positions(pos, g), cfg)
+    y1f = O.token_restore(y1, side, g)
+    y2 = O.block_forward(y1f, w, mod * 2, pos, cfg)
+    got = O.step_forward(x, [w] * 3, [mod, mod * 0.5, mod * 2], pos, cfg, reduction=red)
+    assert np.allclose(got, y2, atol=1e-14)
+
+
+# ------------------------------------------------------------------ int8 block
+
+
+def test_int8_block_close_to_float_block():
+    cfg = O.BlockConfig(d=64, heads=2, head_dim=32, ffn=128, rope_sections=(8, 12, 12))
+    r = np.random.default_rng(15)
+    n = 24
+    w = {"w_qkv": r.standard_normal((3 * 64, 64)) * 0.1, "w_o": r.standard_normal((64, 64)) * 0.1,
+         "w1": r.standard_normal((128, 64)) * 0.1, "w2": r.standard_normal((64, 128)) * 0.1}
+    wq = {}
+    for name, qn, sn in (("w_qkv", "q_qkv", "s_qkv"), ("w_o", "q_o", "s_o"), ("w1", "q1", "s1"), ("w2", "q2", "s2")):
+        wq[qn], s = O.quantize_weight(w[name])
+        wq[sn] = s[:, 0]
+    mod = r.standard_normal((6, 64)) * 0.3
+    x = r.standard_normal((n, 64))
+    pos = r.uniform(0, 5, (n, 3))
+    ref = O.block_forward(x, w, mod, pos, cfg)
+    got = O.block_forward_int8(x, wq, mod, pos, cfg, bf16_storage=False, fc2_group=64)
+    # int8 error on the branch only (x itself passes through exactly)
+    rel = np.linalg.norm((got - x) - (ref - x)) / np.linalg.norm(ref - x)
+    assert rel < 3e-2
+    # fc2 groups equal to F reduce to the per-token scheme
+    a = O.block_forward_int8(x, wq, mod, pos, cfg, bf16_storage=False, fc2_group=128)
+    assert np.linalg.norm((a - x) - (ref - x)) / np.linalg.norm(ref - x) < 3e-2
