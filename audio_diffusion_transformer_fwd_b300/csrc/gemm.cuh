@@ -1,0 +1,250 @@
+// Persistent tcgen05 GEMM for the block's four projections:
+//   C[m][n] = epilogue( sum_k A[m][k] * B[n][k] )     A, B BF16, K-major
+// A = activations [M tokens][K], B = a Linear weight [N out][K in].
+//
+// One CTA per SM walks output tiles of 128 x 256.  Warp 0 streams A/B
+// k-blocks (64 wide) into a 4-deep shared-memory ring with TMA (128-byte
+// swizzle); one thread of warp 1 issues tcgen05.mma (M=128, N=256, K=16)
+// into one of two fp32 TMEM accumulators; warps 2-5 drain the other
+// accumulator through the epilogue, so the epilogue of tile i overlaps the
+// main loop of tile i+1.
+//
+// Epilogues:
+//   kEpiStore  C = bf16(acc)                          (out-projection, FC2)
+//   kEpiGelu   C = bf16(GELU_tanh(acc))               (FC1)
+//   kEpiQKV    3D RoPE on the Q and K thirds, then Q/K stored head-major
+//              [H][M][Dh] and V transposed [H][Dh][ld] for the attention
+//              kernel's K-major operands ([linlog] "h3.c 的核心设计": Q/K/V
+//              routed straight into head-major attention inputs).
+#pragma once
+#include "ptx.cuh"
+
+namespace h3 {
+
+enum { kEpiStore = 0, kEpiGelu = 1, kEpiQKV = 2 };
+
+constexpr int kGemmBM = 128;
+constexpr int kGemmBN = 256;
+constexpr int kGemmBK = 64;
+constexpr int kGemmStages = 4;
+constexpr int kGemmThreads = 192;
+constexpr int kGemmABytes = kGemmBM * kGemmBK * 2;   // 16 KB
+constexpr int kGemmBBytes = kGemmBN * kGemmBK * 2;   // 32 KB
+constexpr int kGemmStageBytes = kGemmABytes + kGemmBBytes;
+constexpr int kGemmTmemCols = 2 * kGemmBN;           // two accumulators
+constexpr int kGemmGroupN = 16;                      // tile raster: bands of 16 N-tiles
+constexpr size_t kGemmSmemBytes = 1024 /*align slack*/ + kGemmStages * kGemmStageBytes + 256;
+
+struct GemmArgs {
+  int M, N, K;
+  int tiles_m, tiles_n, num_tiles;
+  __nv_bfloat16* c;   // kEpiStore / kEpiGelu
+  int ldc;
+  // kEpiQKV
+  __nv_bfloat16* q;
+  __nv_bfloat16* k;
+  __nv_bfloat16* vt;
+  int vt_ld;
+  int d;
+  int head_dim;
+  const float2* rope;  // [M][head_dim/2] (cos, sin)
+};
+
+__device__ __forceinline__ float gelu_tanh_f(float x) {
+  const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
+  const float k1 = 0.044715f;
+  return 0.5f * x * (1.0f + tanhf(k0 * (x + k1 * x * x * x)));
+}
+
+__device__ __forceinline__ void gemm_tile_coords(int t, const GemmArgs& a, int& mb, int& nb) {
+  const int per_group = kGemmGroupN * a.tiles_m;
+  const int g = t / per_group;
+  const int r = t - g * per_group;
+  const int n_first = g * kGemmGroupN;
+  const int gn = min(kGemmGroupN, a.tiles_n - n_first);
+  mb = r / gn;
+  nb = n_first + (r - mb * gn);
+}
+
+template <int EPI>
+__device__ __forceinline__ void gemm_epilogue_chunk(const GemmArgs& a, float (&v)[32], int grow,
+                                                    int gcol) {
+  if (grow >= a.M) return;
+  if (EPI == kEpiStore || EPI == kEpiGelu) {
+    uint32_t p[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float x0 = v[2 * i], x1 = v[2 * i + 1];
+      if (EPI == kEpiGelu) {
+        x0 = gelu_tanh_f(x0);
+        x1 = gelu_tanh_f(x1);
+      }
+      p[i] = pack_bf16x2(x0, x1);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(a.c + static_cast<size_t>(grow) * a.ldc + gcol);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+  } else {
+    const int region = gcol / a.d;          // 0 = Q, 1 = K, 2 = V
+    const int cin = gcol - region * a.d;
+    const int head = cin / a.head_dim;
+    const int dh0 = cin - head * a.head_dim;
+    if (region < 2) {
+      const float4* cs = reinterpret_cast<const float4*>(
+          a.rope + static_cast<size_t>(grow) * (a.head_dim / 2) + dh0 / 2);
+      uint32_t p[16];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 t = __ldg(cs + i);   // (cos, sin) of two consecutive pairs
+        const float a0 = v[4 * i], b0 = v[4 * i + 1], a1 = v[4 * i + 2], b1 = v[4 * i + 3];
+        p[2 * i] = pack_bf16x2(a0 * t.x - b0 * t.y, a0 * t.y + b0 * t.x);
+        p[2 * i + 1] = pack_bf16x2(a1 * t.z - b1 * t.w, a1 * t.w + b1 * t.z);
+      }
+      __nv_bfloat16* base = region == 0 ? a.q : a.k;
+      uint4* dst = reinterpret_cast<uint4*>(
+          base + (static_cast<size_t>(head) * a.M + grow) * a.head_dim + dh0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+    } else {
+      __nv_bfloat16* dst = a.vt + (static_cast<size_t>(head) * a.head_dim + dh0) * a.vt_ld + grow;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) dst[static_cast<size_t>(i) * a.vt_ld] = __float2bfloat16_rn(v[i]);
+    }
+  }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kGemmStages * kGemmABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kGemmStages * kGemmStageBytes);
+  // bars: full[S], empty[S], tfull[2], tempty[2], drain
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kGemmStages + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = smem_u32(bars + kGemmStages);
+  const uint32_t tfull0 = smem_u32(bars + 2 * kGemmStages);
+  const uint32_t tempty0 = smem_u32(bars + 2 * kGemmStages + 2);
+  const uint32_t drain = smem_u32(bars + 2 * kGemmStages + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kGemmStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(tfull0 + 8 * i, 1);
+      mbar_init(tempty0 + 8 * i, 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), kGemmTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int kblocks = args.K / kGemmBK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
+        int mb, nb;
+        gemm_tile_coords(t, args, mb, nb);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
+          const uint32_t fb = full0 + 8 * stage;
+          mbar_arrive_expect_tx(fb, kGemmStageBytes);
+          tma_load_2d(smem_u32(sA + stage * kGemmABytes), &tmA, fb, kb * kGemmBK, mb * kGemmBM);
+          tma_load_2d(smem_u32(sB + stage * kGemmBBytes), &tmB, fb, kb * kGemmBK, nb * kGemmBN);
+          if (++stage == kGemmStages) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!ok) {
+        // let loads already in flight land before the CTA exits
+        for (int s = 0; s < kGemmStages; ++s) mbar_wait_drain(full0 + 8 * s, phase);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(kGemmBM, kGemmBN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x, ++it) {
+        const int acc = it & 1;
+        if (!mbar_wait(tempty0 + 8 * acc, ((it >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kGemmBN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * kGemmABytes);
+          const uint32_t b0 = smem_u32(sB + stage * kGemmBBytes);
+#pragma unroll
+          for (int k = 0; k < kGemmBK / 16; ++k) {
+            tc_mma_bf16(d_tmem, sdesc_k128(a0 + 32 * k), sdesc_k128(b0 + 32 * k), idesc,
+                        (kb | k) != 0);
+          }
+          tc_commit(empty0 + 8 * stage);
+          if (++stage == kGemmStages) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit(tfull0 + 8 * acc);
+      }
+      // every MMA issued by this thread has completed once `drain` flips
+      tc_commit(drain);
+      mbar_wait_drain(drain, 0);
+    }
+  } else {
+    // ---------------- epilogue warps 2..5: TMEM lane quarter = warp % 4
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    int it = 0;
+    for (int t = blockIdx.x; t < args.num_tiles; t += gridDim.x, ++it) {
+      int mb, nb;
+      gemm_tile_coords(t, args, mb, nb);
+      const int acc = it & 1;
+      if (!mbar_wait(tfull0 + 8 * acc, (it >> 1) & 1, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kGemmBN;
+      const int grow = mb * kGemmBM + row;
+#pragma unroll 1
+      for (int c = 0; c < kGemmBN / 32; ++c) {
+        float v[32];
+        tmem_ld32(tbase + c * 32, v);
+        gemm_epilogue_chunk<EPI>(args, v, grow, nb * kGemmBN + c * 32);
+      }
+      tc_fence_before();
+      mbar_arrive(tempty0 + 8 * acc);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, kGemmTmemCols);
+}
+
+}  // namespace h3

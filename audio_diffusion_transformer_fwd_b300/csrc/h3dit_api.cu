@@ -1,0 +1,728 @@
+// C ABI of libh3dit.so: argument checks, workspace layout, tensor maps,
+// kernel launches and the block / step sequencing.  The whole library is
+// this one translation unit (the kernel files are included below).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/h3dit.h"
+#include "attention.cuh"
+#include "gemm.cuh"
+#include "ptx.cuh"
+#include "rows.cuh"
+
+namespace {
+
+using bf16 = __nv_bfloat16;
+
+thread_local std::string t_last_error;
+
+h3dit_status fail(h3dit_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return st;
+}
+
+#define H3_CUDA(call)                                                                 \
+  do {                                                                                \
+    cudaError_t e_ = (call);                                                          \
+    if (e_ != cudaSuccess)                                                            \
+      return fail(H3DIT_E_CUDA, "%s: %s (%s:%d)", #call, cudaGetErrorString(e_),     \
+                  __FILE__, __LINE__);                                                \
+  } while (0)
+
+#define H3_TRY(expr)                       \
+  do {                                     \
+    h3dit_status s_ = (expr);              \
+    if (s_ != H3DIT_OK) return s_;         \
+  } while (0)
+
+// ------------------------------------------------------------------ timing
+enum KernelClass { kRows = 0, kQKV = 1, kAttn = 2, kOProj = 3, kFC1 = 4, kFC2 = 5, kReduce = 6, kQuant = 7, kNumClasses = 8 };
+
+struct Timing {
+  std::mutex mu;
+  bool enabled = false;
+  struct Pending { int cls; cudaEvent_t a, b; };
+  std::vector<Pending> pending;
+  double total_ms[kNumClasses] = {0};
+  long long count[kNumClasses] = {0};
+} g_timing;
+
+struct TimedLaunch {
+  int cls;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr, b = nullptr;
+  TimedLaunch(int c, cudaStream_t st) : cls(c), s(st) {
+    if (!g_timing.enabled) return;
+    cudaEventCreate(&a);
+    cudaEventCreate(&b);
+    cudaEventRecord(a, s);
+  }
+  ~TimedLaunch() {
+    if (!a) return;
+    cudaEventRecord(b, s);
+    std::lock_guard<std::mutex> lk(g_timing.mu);
+    g_timing.pending.push_back({cls, a, b});
+  }
+};
+
+// ------------------------------------------------------------------ device facts
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 148;
+  }
+  return cached[dev];
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+h3dit_status get_encoder(EncodeTiledFn* out) {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+    if (err == cudaSuccess && q == cudaDriverEntryPointSuccess) fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  if (!fn) return fail(H3DIT_E_CUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorString(err));
+  *out = fn;
+  return H3DIT_OK;
+}
+
+// BF16 tensor map with the 128-byte swizzle; dims/strides innermost first,
+// strides in bytes for dims 1.. ; out-of-bounds boxes read zeros.
+h3dit_status make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                      const uint64_t* strides, const uint32_t* box) {
+  EncodeTiledFn enc;
+  H3_TRY(get_encoder(&enc));
+  cuuint64_t gd[3], gs[2];
+  cuuint32_t bx[3], es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) { gd[i] = dims[i]; bx[i] = box[i]; }
+  for (int i = 0; i < rank - 1; ++i) gs[i] = strides[i];
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gd, gs, bx, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(H3DIT_E_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return H3DIT_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ------------------------------------------------------------------ config checks
+h3dit_status check_cfg(const h3dit_config* c) {
+  if (!c) return fail(H3DIT_E_INVAL, "config is NULL");
+  if (c->d <= 0 || c->heads <= 0 || c->head_dim <= 0 || c->ffn <= 0)
+    return fail(H3DIT_E_INVAL, "non-positive block size");
+  if (c->heads * c->head_dim != c->d) return fail(H3DIT_E_INVAL, "heads*head_dim != d");
+  if (c->head_dim != 64 && c->head_dim != 128)
+    return fail(H3DIT_E_UNSUPPORTED, "head_dim %d (64 or 128 supported)", c->head_dim);
+  if (c->d % 256 != 0 || c->d > 8192) return fail(H3DIT_E_UNSUPPORTED, "d %d (multiple of 256, <= 8192)", c->d);
+  if (c->ffn % 256 != 0) return fail(H3DIT_E_UNSUPPORTED, "ffn %d (multiple of 256)", c->ffn);
+  int s = 0;
+  for (int i = 0; i < 3; ++i) {
+    if (c->rope_sections[i] < 0 || c->rope_sections[i] % 2 != 0)
+      return fail(H3DIT_E_INVAL, "rope section %d must be even and >= 0", i);
+    s += c->rope_sections[i];
+  }
+  if (s != c->head_dim) return fail(H3DIT_E_INVAL, "rope sections sum %d != head_dim %d", s, c->head_dim);
+  if (!(c->eps > 0.f)) return fail(H3DIT_E_INVAL, "eps must be > 0");
+  if (!(c->rope_theta > 0.f)) return fail(H3DIT_E_INVAL, "rope_theta must be > 0");
+  if (c->precision != H3DIT_BF16 && c->precision != H3DIT_INT8)
+    return fail(H3DIT_E_INVAL, "precision %d", c->precision);
+  return H3DIT_OK;
+}
+
+// Attention alone needs only the head layout.
+h3dit_status check_heads(const h3dit_config* c) {
+  if (!c) return fail(H3DIT_E_INVAL, "config is NULL");
+  if (c->heads <= 0 || c->head_dim <= 0) return fail(H3DIT_E_INVAL, "non-positive head layout");
+  if (c->head_dim != 64 && c->head_dim != 128)
+    return fail(H3DIT_E_UNSUPPORTED, "head_dim %d (64 or 128 supported)", c->head_dim);
+  if (c->d != c->heads * c->head_dim) return fail(H3DIT_E_INVAL, "heads*head_dim != d");
+  return H3DIT_OK;
+}
+
+h3dit_status check_grid(const h3dit_video_grid* g, int n_tokens) {
+  if (!g) return fail(H3DIT_E_INVAL, "video grid is NULL");
+  if (g->offset < 0 || g->T < 0 || g->Hh < 0 || g->W < 0)
+    return fail(H3DIT_E_INVAL, "negative video grid field");
+  const long long nv = 1LL * g->T * g->Hh * g->W;
+  if (g->offset + nv > n_tokens) return fail(H3DIT_E_INVAL, "video grid exceeds the %d rows", n_tokens);
+  return H3DIT_OK;
+}
+
+h3::PairGrid pair_grid(const h3dit_video_grid* g, int n_tokens) {
+  h3::PairGrid p;
+  p.offset = g->offset;
+  p.T = g->T;
+  p.Hh = g->Hh;
+  p.W = g->W;
+  p.Wr = (g->W + 1) / 2;
+  p.n_full = n_tokens;
+  p.n_red = n_tokens - g->T * g->Hh * (g->W - p.Wr);
+  return p;
+}
+
+// ------------------------------------------------------------------ launches
+template <typename K>
+h3dit_status set_smem(K kernel, size_t bytes) {
+  H3_CUDA(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes));
+  return H3DIT_OK;
+}
+
+h3dit_status launch_gemm(int epi, const void* A, const void* B, int M, int N, int K, h3::GemmArgs args,
+                         int cls, cudaStream_t s) {
+  if (M < 1 || N % h3::kGemmBN != 0 || K % h3::kGemmBK != 0 || N <= 0 || K <= 0)
+    return fail(H3DIT_E_UNSUPPORTED, "gemm shape %dx%dx%d (n %% 256, k %% 64)", M, N, K);
+  if (!aligned(A, 16) || !aligned(B, 16)) return fail(H3DIT_E_INVAL, "gemm operands must be 16-byte aligned");
+  CUtensorMap ta, tb;
+  {
+    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)M};
+    const uint64_t str[1] = {(uint64_t)K * 2};
+    const uint32_t box[2] = {h3::kGemmBK, h3::kGemmBM};
+    H3_TRY(make_map(&ta, A, 2, dims, str, box));
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)N};
+    const uint64_t str[1] = {(uint64_t)K * 2};
+    const uint32_t box[2] = {h3::kGemmBK, h3::kGemmBN};
+    H3_TRY(make_map(&tb, B, 2, dims, str, box));
+  }
+  args.M = M;
+  args.N = N;
+  args.K = K;
+  args.tiles_m = (M + h3::kGemmBM - 1) / h3::kGemmBM;
+  args.tiles_n = N / h3::kGemmBN;
+  args.num_tiles = args.tiles_m * args.tiles_n;
+  const int grid = std::min(args.num_tiles, sm_count());
+  TimedLaunch tl(cls, s);
+  switch (epi) {
+    case h3::kEpiStore: {
+      static bool once = false;
+      if (!once) { H3_TRY(set_smem(h3::gemm_bf16_tc_kernel<h3::kEpiStore>, h3::kGemmSmemBytes)); once = true; }
+      h3::gemm_bf16_tc_kernel<h3::kEpiStore><<<grid, h3::kGemmThreads, h3::kGemmSmemBytes, s>>>(ta, tb, args);
+      break;
+    }
+    case h3::kEpiGelu: {
+      static bool once = false;
+      if (!once) { H3_TRY(set_smem(h3::gemm_bf16_tc_kernel<h3::kEpiGelu>, h3::kGemmSmemBytes)); once = true; }
+      h3::gemm_bf16_tc_kernel<h3::kEpiGelu><<<grid, h3::kGemmThreads, h3::kGemmSmemBytes, s>>>(ta, tb, args);
+      break;
+    }
+    case h3::kEpiQKV: {
+      static bool once = false;
+      if (!once) { H3_TRY(set_smem(h3::gemm_bf16_tc_kernel<h3::kEpiQKV>, h3::kGemmSmemBytes)); once = true; }
+      h3::gemm_bf16_tc_kernel<h3::kEpiQKV><<<grid, h3::kGemmThreads, h3::kGemmSmemBytes, s>>>(ta, tb, args);
+      break;
+    }
+    default:
+      return fail(H3DIT_E_INVAL, "unknown epilogue %d", epi);
+  }
+  H3_CUDA(cudaGetLastError());
+  return H3DIT_OK;
+}
+
+h3dit_status launch_attention(const h3dit_config* c, const void* q, const void* k, const void* vt, int vt_ld,
+                              int n, void* o, cudaStream_t s) {
+  const int dh = c->head_dim, H = c->heads;
+  if (vt_ld < n || vt_ld % 8 != 0) return fail(H3DIT_E_INVAL, "vt_ld %d (>= n, multiple of 8)", vt_ld);
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(vt, 16) || !aligned(o, 16))
+    return fail(H3DIT_E_INVAL, "attention tensors must be 16-byte aligned");
+  CUtensorMap tq, tk, tv;
+  {
+    const uint64_t dims[3] = {(uint64_t)dh, (uint64_t)n, (uint64_t)H};
+    const uint64_t str[2] = {(uint64_t)dh * 2, (uint64_t)n * dh * 2};
+    const uint32_t box[3] = {64, h3::kAttnBQ, 1};
+    H3_TRY(make_map(&tq, q, 3, dims, str, box));
+    H3_TRY(make_map(&tk, k, 3, dims, str, box));
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)n, (uint64_t)dh, (uint64_t)H};
+    const uint64_t str[2] = {(uint64_t)vt_ld * 2, (uint64_t)dh * vt_ld * 2};
+    const uint32_t box[3] = {64, (uint32_t)dh, 1};
+    H3_TRY(make_map(&tv, vt, 3, dims, str, box));
+  }
+  h3::AttnArgs a;
+  a.n = n;
+  a.heads = H;
+  a.o = static_cast<bf16*>(o);
+  a.scale_log2 = 1.4426950408889634f / sqrtf((float)dh);
+  dim3 grid((n + h3::kAttnBQ - 1) / h3::kAttnBQ, H);
+  TimedLaunch tl(kAttn, s);
+  if (dh == 128) {
+    static bool once = false;
+    if (!once) { H3_TRY(set_smem(h3::attn_fwd_tc_kernel<128>, h3::AttnSmem<128>::kTotal)); once = true; }
+    h3::attn_fwd_tc_kernel<128><<<grid, h3::kAttnThreads, h3::AttnSmem<128>::kTotal, s>>>(tq, tk, tv, a);
+  } else {
+    static bool once = false;
+    if (!once) { H3_TRY(set_smem(h3::attn_fwd_tc_kernel<64>, h3::AttnSmem<64>::kTotal)); once = true; }
+    h3::attn_fwd_tc_kernel<64><<<grid, h3::kAttnThreads, h3::AttnSmem<64>::kTotal, s>>>(tq, tk, tv, a);
+  }
+  H3_CUDA(cudaGetLastError());
+  return H3DIT_OK;
+}
+
+bool fusion_disabled() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("H3DIT_DISABLE_GATED_ADALN");
+    v = (e && e[0] && e[0] != '0') ? 1 : 0;
+  }
+  return v == 1;
+}
+
+h3dit_status launch_rows(void* x, const void* branch, const float* gate, const float* shift, const float* scale,
+                         void* h, int n, int d, float eps, cudaStream_t s) {
+  TimedLaunch tl(kRows, s);
+  bf16* xb = static_cast<bf16*>(x);
+  const bf16* bb = static_cast<const bf16*>(branch);
+  bf16* hb = static_cast<bf16*>(h);
+  const bool gate_on = branch != nullptr;
+  const bool norm_on = shift != nullptr;
+  if (gate_on && norm_on && !fusion_disabled()) {
+    h3::gate_adaln_kernel<true, true><<<n, h3::kRowThreads, 0, s>>>(xb, bb, gate, shift, scale, hb, d, eps);
+  } else {
+    if (gate_on)
+      h3::gate_adaln_kernel<true, false><<<n, h3::kRowThreads, 0, s>>>(xb, bb, gate, nullptr, nullptr, nullptr, d, eps);
+    if (norm_on)
+      h3::gate_adaln_kernel<false, true><<<n, h3::kRowThreads, 0, s>>>(xb, nullptr, nullptr, shift, scale, hb, d, eps);
+  }
+  H3_CUDA(cudaGetLastError());
+  return H3DIT_OK;
+}
+
+h3dit_status launch_rope_table(const h3dit_config* c, const float* pos, int n, float* table, cudaStream_t s) {
+  TimedLaunch tl(kRows, s);
+  h3::RopeSpec rs;
+  rs.head_dim = c->head_dim;
+  for (int i = 0; i < 3; ++i) rs.sec[i] = c->rope_sections[i];
+  rs.theta = c->rope_theta;
+  const int total = n * (c->head_dim / 2);
+  h3::rope_table_kernel<<<(total + 255) / 256, 256, 0, s>>>(pos, n, rs, reinterpret_cast<float2*>(table));
+  H3_CUDA(cudaGetLastError());
+  return H3DIT_OK;
+}
+
+// ------------------------------------------------------------------ workspace
+struct Arena {
+  size_t a1 = 0, a2 = 0, a3 = 0, rope = 0;     // offsets
+  size_t xred = 0, rope_red = 0, pos_red = 0;  // reduction extras
+  size_t total = 0;
+  int vt_ld = 0;
+};
+
+// Activation arenas aliased by lifetime ([linlog] "DiT 融合内核", activation
+// buffer aliasing):  a1 holds Q, K, V^T and then the FC1 output u; a2 holds
+// h, then the attention output o, then h2, then the next block's h; a3 holds
+// the out-projection output and then the FC2 output.
+Arena plan_arena(const h3dit_config* c, int n, const h3dit_reduction* tr) {
+  Arena a;
+  const size_t d = c->d, F = c->ffn;
+  a.vt_ld = (int)round_up((size_t)n, 64);
+  const size_t qk = round_up(n * d * 2, 256);
+  const size_t vt = round_up((size_t)c->heads * c->head_dim * a.vt_ld * 2, 256);
+  const size_t a1 = std::max(2 * qk + vt, round_up(n * F * 2, 256));
+  const size_t nd = round_up(n * d * 2, 256);
+  size_t off = 0;
+  a.a1 = off; off += a1;
+  a.a2 = off; off += nd;
+  a.a3 = off; off += nd;
+  a.rope = off; off += round_up((size_t)n * (c->head_dim / 2) * 8, 256);
+  if (tr) {
+    const h3::PairGrid g = pair_grid(&tr->grid, n);
+    a.xred = off; off += round_up((size_t)g.n_red * d * 2, 256);
+    a.rope_red = off; off += round_up((size_t)g.n_red * (c->head_dim / 2) * 8, 256);
+    a.pos_red = off; off += round_up((size_t)g.n_red * 3 * 4, 256);
+  }
+  a.total = off;
+  return a;
+}
+
+struct BlockBufs {
+  uint8_t* base;
+  Arena ar;
+};
+
+// Runs one block's sub-steps from its AdaLN output (already in a2) to the
+// final gated residual.  next_shift/next_scale: the following block's AdaLN-1
+// vectors to emit into a2 from the residual kernel, or NULL.
+h3dit_status run_block_body(const h3dit_config* c, const h3dit_block_weights* w, const float* mod, bf16* x,
+                            int n, const float* rope, const BlockBufs& B, int vt_ld,
+                            const float* next_shift, const float* next_scale, cudaStream_t s) {
+  const int d = c->d, F = c->ffn, H = c->heads, dh = c->head_dim;
+  uint8_t* a1 = B.base + B.ar.a1;
+  bf16* a2 = reinterpret_cast<bf16*>(B.base + B.ar.a2);
+  bf16* a3 = reinterpret_cast<bf16*>(B.base + B.ar.a3);
+  bf16* q = reinterpret_cast<bf16*>(a1);
+  bf16* k = reinterpret_cast<bf16*>(a1 + round_up((size_t)n * d * 2, 256));
+  bf16* vt = reinterpret_cast<bf16*>(a1 + 2 * round_up((size_t)n * d * 2, 256));
+  bf16* u = reinterpret_cast<bf16*>(a1);
+  const float* gate1 = mod + 2 * d;
+  const float* shift2 = mod + 3 * d;
+  const float* scale2 = mod + 4 * d;
+  const float* gate2 = mod + 5 * d;
+
+  h3::GemmArgs g{};
+  g.q = q; g.k = k; g.vt = vt; g.vt_ld = vt_ld; g.d = d; g.head_dim = dh;
+  g.rope = reinterpret_cast<const float2*>(rope);
+  H3_TRY(launch_gemm(h3::kEpiQKV, a2, w->w_qkv, n, 3 * d, d, g, kQKV, s));
+  H3_TRY(launch_attention(c, q, k, vt, vt_ld, n, a2, s));
+  h3::GemmArgs go{};
+  go.c = a3; go.ldc = d;
+  H3_TRY(launch_gemm(h3::kEpiStore, a2, w->w_o, n, d, d, go, kOProj, s));
+  H3_TRY(launch_rows(x, a3, gate1, shift2, scale2, a2, n, d, c->eps, s));
+  h3::GemmArgs g1{};
+  g1.c = u; g1.ldc = F;
+  H3_TRY(launch_gemm(h3::kEpiGelu, a2, w->w1, n, F, d, g1, kFC1, s));
+  h3::GemmArgs g2{};
+  g2.c = a3; g2.ldc = d;
+  H3_TRY(launch_gemm(h3::kEpiStore, u, w->w2, n, d, F, g2, kFC2, s));
+  H3_TRY(launch_rows(x, a3, gate2, next_shift, next_scale, a2, n, d, c->eps, s));
+  (void)H;
+  return H3DIT_OK;
+}
+
+h3dit_status check_weights(const h3dit_config* c, const h3dit_block_weights* w) {
+  if (!w) return fail(H3DIT_E_INVAL, "weights are NULL");
+  if (!w->w_qkv || !w->w_o || !w->w1 || !w->w2) return fail(H3DIT_E_INVAL, "a weight pointer is NULL");
+  if (c->precision == H3DIT_INT8) {
+    if (!w->s_qkv || !w->s_o || !w->s1 || !w->s2) return fail(H3DIT_E_INVAL, "int8 weights need scales");
+  }
+  return H3DIT_OK;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+extern "C" {
+
+const char* h3dit_last_error(void) { return t_last_error.c_str(); }
+
+int h3dit_version(void) { return H3DIT_VERSION; }
+
+h3dit_status h3dit_check_device_error(cudaStream_t stream) {
+  H3_CUDA(cudaStreamSynchronize(stream));
+  unsigned int v = 0, zero = 0;
+  H3_CUDA(cudaMemcpyFromSymbol(&v, h3::g_device_error, sizeof(v)));
+  if (v) {
+    H3_CUDA(cudaMemcpyToSymbol(h3::g_device_error, &zero, sizeof(zero)));
+    return fail(H3DIT_E_TIMEOUT, "a kernel's pipeline wait ran out of time (device error word 0x%x)", v);
+  }
+  return H3DIT_OK;
+}
+
+h3dit_status h3dit_timing_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_timing.mu);
+  g_timing.enabled = on != 0;
+  return H3DIT_OK;
+}
+
+h3dit_status h3dit_timing_reset(void) {
+  std::lock_guard<std::mutex> lk(g_timing.mu);
+  for (auto& p : g_timing.pending) {
+    cudaEventSynchronize(p.b);
+    cudaEventDestroy(p.a);
+    cudaEventDestroy(p.b);
+  }
+  g_timing.pending.clear();
+  for (int i = 0; i < kNumClasses; ++i) { g_timing.total_ms[i] = 0; g_timing.count[i] = 0; }
+  return H3DIT_OK;
+}
+
+h3dit_status h3dit_timing_read(int cls, double* total_ms, long long* launches) {
+  if (cls < 0 || cls >= kNumClasses || !total_ms || !launches) return fail(H3DIT_E_INVAL, "bad timing query");
+  std::lock_guard<std::mutex> lk(g_timing.mu);
+  for (auto& p : g_timing.pending) {
+    H3_CUDA(cudaEventSynchronize(p.b));
+    float ms = 0.f;
+    H3_CUDA(cudaEventElapsedTime(&ms, p.a, p.b));
+    g_timing.total_ms[p.cls] += ms;
+    g_timing.count[p.cls] += 1;
+    cudaEventDestroy(p.a);
+    cudaEventDestroy(p.b);
+  }
+  g_timing.pending.clear();
+  *total_ms = g_timing.total_ms[cls];
+  *launches = g_timing.count[cls];
+  return H3DIT_OK;
+}
+
+h3dit_status h3dit_workspace_size(const h3dit_config* cfg, int n_tokens, const h3dit_reduction* tr,
+                                  size_t* bytes) {
+  H3_TRY(check_cfg(cfg));
+  if (!bytes) return fail(H3DIT_E_INVAL, "bytes is NULL");
+  if (n_tokens < 1) return fail(H3DIT_E_INVAL, "n_tokens %d", n_tokens);
+  if (tr) H3_TRY(check_grid(&tr->grid, n_tokens));
+  *bytes = plan_arena(cfg, n_tokens, tr).total;
+  return H3DIT_OK;
+}
+
+h3dit_status h3dit_rope_table(const h3dit_config* cfg, const float* pos, int n_tokens, float* table,
+                              cudaStream_t stream) {
+  H3_TRY(check_cfg(cfg));
+  if (!pos || !table) return fail(H3DIT_E_INVAL, "NULL pointer");
+  if (n_tokens < 1) return fail(H3DIT_E_INVAL, "n_tokens %d", n_tokens);
+  return launch_rope_table(cfg, pos, n_tokens, table, stream);
+}
+
+h3dit_status h3dit_adaln(const h3dit_config* cfg, const void* x, const float* shift, const float* scale,
+                         int n_tokens, void* h, cudaStream_t stream) {
+  H3_TRY(check_cfg(cfg));
+  if (!x || !shift || !scale || !h) return fail(H3DIT_E_INVAL, "NULL pointer");
+  if (n_tokens < 1) return fail(H3DIT_E_INVAL, "n_tokens %d", n_tokens);
+  return launch_rows(const_cast<void*>(x), nullptr, nullptr, shift, scale, h, n_tokens, cfg->d, cfg->eps, stream);
+}
+
+h3dit_status h3dit_gate_residual_adaln(const h3dit_config* cfg, void* x, const void* branch, const float* gate,
+                                       const float* shift, const float* scale, int n_tokens, void* h,
+                                       cudaStream_t stream) {
+  H3_TRY(check_cfg(cfg));
+  if (!x || !branch || !gate) return fail(H3DIT_E_INVAL, "NULL pointer");
+  if ((shift == nullptr) != (scale == nullptr)) return fail(H3DIT_E_INVAL, "shift and scale must both be set or NULL");
+  if (shift && !h) return fail(H3DIT_E_INVAL, "h is NULL");
+  if (n_tokens < 1) return fail(H3DIT_E_INVAL, "n_tokens %d", n_tokens);
+  return launch_rows(x, branch, gate, shift, scale, h, n_tokens, cfg->d, cfg->eps, stream);
+}
+
+h3dit_status h3dit_qkv_project(const h3dit_config* cfg, const void* h, const void* w_qkv, const float* table,
+                               int n_tokens, void* q, void* k, void* vt, int vt_ld, cudaStream_t stream) {
+  H3_TRY(check_cfg(cfg));
+  if (!h || !w_qkv || !table || !q || !k || !vt) return fail(H3DIT_E_INVAL, "NULL pointer");
+  if (n_tokens < 1) return fail(H3DIT_E_INVAL, "n_tokens %d", n_tokens);
+  if (vt_ld < n_tokens || vt_ld % 8 != 0) return fail(H3DIT_E_INVAL, "vt_ld %d", vt_ld);
+  if (!aligned(table, 16) || !aligned(q, 16) || !aligned(k, 16) || !aligned(vt, 16))
+    return fail(H3DIT_E_INVAL, "outputs must be 16-byte aligned");
+  h3::GemmArgs g{};
+  g.q = static_cast<bf16*>(q);
+  g.k = static_cast<bf16*>(k);
+  g.vt = static_cast<bf16*>(vt);
+  g.vt_ld = vt_ld;
+  g.d = cfg->d;
+  g.head_dim = cfg->head_dim;
+  g.rope = reinterpret_cast<const float2*>(table);
+  return launch_gemm(h3::kEpiQKV, h, w_qkv, n_tokens, 3 * cfg->d, cfg->d, g, kQKV, stream);
+}
+
+h3dit_status h3dit_attention(const h3dit_config* cfg, const void* q, const void* k, const void* vt, int vt_ld,
+                             int n_tokens, void* o, cudaStream_t stream) {
+  H3_TRY(check_heads(cfg));
+  if (!q || !k || !vt || !o) return fail(H3DIT_E_INVAL, "NULL pointer");
+  if (n_tokens < 1) return fail(H3DIT_E_INVAL, "n_tokens %d", n_tokens);
+  return launch_attention(cfg, q, k, vt, vt_ld, n_tokens, o, stream);
+}
+
+h3dit_status h3dit_linear(const void* a, const void* b, int m, int n, int k, int act, void* c,
+                          cudaStream_t stream) {
+  if (!a || !b || !c) return fail(H3DIT_E_INVAL, "NULL pointer");
+  if (m < 1 || n < 1 || k < 1) return fail(H3DIT_E_INVAL, "non-positive shape");
+  if (act != 0 && act != 1) return fail(H3DIT_E_INVAL, "act %d", act);
+  if (!aligned(c, 16)) return fail(H3DIT_E_INVAL, "c must be 16-byte aligned");
+  h3::GemmArgs g{};
+  g.c = static_cast<bf16*>(c);
+  g.ldc = n;
+  return launch_gemm(act ? h3::kEpiGelu : h3::kEpiStore, a, b, m, n, k, g, act ? kFC1 : kOProj, stream);
+}
+
+h3dit_status h3dit_block_forward(const h3dit_config* cfg, const h3dit_block_weights* w, const float* mod,
+                                 void* x, const float* pos, int n_tokens, void* ws, size_t ws_bytes,
+                                 cudaStream_t stream) {
+  H3_TRY(check_cfg(cfg));
+  H3_TRY(check_weights(cfg, w));
+  if (!mod || !x || !pos || !ws) return fail(H3DIT_E_INVAL, "NULL pointer");
+  if (n_tokens < 1) return fail(H3DIT_E_INVAL, "n_tokens %d", n_tokens);
+  if (cfg->precision != H3DIT_BF16) return fail(H3DIT_E_UNSUPPORTED, "int8 block not built yet");
+  if (!aligned(ws, 256) || !aligned(x, 16)) return fail(H3DIT_E_INVAL, "ws must be 256-byte and x 16-byte aligned");
+  const Arena ar = plan_arena(cfg, n_tokens, nullptr);
+  if (ws_bytes < ar.total) return fail(H3DIT_E_NOMEM, "workspace %zu < %zu bytes", ws_bytes, ar.total);
+  BlockBufs B{static_cast<uint8_t*>(ws), ar};
+  float* rope = reinterpret_cast<float*>(B.base + ar.rope);
+  bf16* xb = static_cast<bf16*>(x);
+  const int d = cfg->d;
+  H3_TRY(launch_rope_table(cfg, pos, n_tokens, rope, stream));
+  H3_TRY(launch_rows(xb, nullptr, nullptr, mod + 0 * d, mod + 1 * d, B.base + ar.a2, n_tokens, d, cfg->eps, stream));
+  return run_block_body(cfg, w, mod, xb, n_tokens, rope, B, ar.vt_ld, nullptr, nullptr, stream);
+}
+
+h3dit_status h3dit_step_forward(const h3dit_config* cfg, const h3dit_block_weights* w, int n_blocks,
+                                const float* mods, void* x, const float* pos, int n_tokens,
+                                const h3dit_reduction* tr, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  H3_TRY(check_cfg(cfg));
+  if (!w || n_blocks < 0) return fail(H3DIT_E_INVAL, "weights NULL or n_blocks < 0");
+  if (n_blocks == 0) return H3DIT_OK;
+  for (int b = 0; b < n_blocks; ++b) H3_TRY(check_weights(cfg, &w[b]));
+  if (!mods || !x || !pos || !ws) return fail(H3DIT_E_INVAL, "NULL pointer");
+  if (n_tokens < 1) return fail(H3DIT_E_INVAL, "n_tokens %d", n_tokens);
+  if (cfg->precision != H3DIT_BF16) return fail(H3DIT_E_UNSUPPORTED, "int8 step not built yet");
+  if (!aligned(ws, 256) || !aligned(x, 16)) return fail(H3DIT_E_INVAL, "ws must be 256-byte and x 16-byte aligned");
+  if (tr) {
+    H3_TRY(check_grid(&tr->grid, n_tokens));
+    if (tr->reduce_after_block < 0 || tr->restore_before_block <= tr->reduce_after_block)
+      return fail(H3DIT_E_INVAL, "reduction blocks %d / %d", tr->reduce_after_block, tr->restore_before_block);
+  }
+  const Arena ar = plan_arena(cfg, n_tokens, tr);
+  if (ws_bytes < ar.total) return fail(H3DIT_E_NOMEM, "workspace %zu < %zu bytes", ws_bytes, ar.total);
+  BlockBufs B{static_cast<uint8_t*>(ws), ar};
+  const int d = cfg->d;
+  bf16* xfull = static_cast<bf16*>(x);
+  float* rope_full = reinterpret_cast<float*>(B.base + ar.rope);
+  H3_TRY(launch_rope_table(cfg, pos, n_tokens, rope_full, stream));
+
+  h3::PairGrid pg{};
+  bf16* xred = nullptr;
+  float* rope_red = nullptr;
+  if (tr) {
+    pg = pair_grid(&tr->grid, n_tokens);
+    xred = reinterpret_cast<bf16*>(B.base + ar.xred);
+    rope_red = reinterpret_cast<float*>(B.base + ar.rope_red);
+    const float* pr = tr->pos_reduced;
+    if (!pr) {
+      float* p = reinterpret_cast<float*>(B.base + ar.pos_red);
+      TimedLaunch tl(kReduce, stream);
+      h3::reduced_positions_kernel<<<(pg.n_red + 127) / 128, 128, 0, stream>>>(pos, pg, p);
+      H3_CUDA(cudaGetLastError());
+      pr = p;
+    }
+    H3_TRY(launch_rope_table(cfg, pr, pg.n_red, rope_red, stream));
+  }
+
+  bf16* cur = xfull;
+  int cur_n = n_tokens;
+  const float* cur_rope = rope_full;
+  bool reduced = false;
+  H3_TRY(launch_rows(cur, nullptr, nullptr, mods, mods + d, B.base + ar.a2, cur_n, d, cfg->eps, stream));
+  for (int b = 0; b < n_blocks; ++b) {
+    const float* mod = mods + (size_t)6 * d * b;
+    const bool last = b + 1 == n_blocks;
+    const bool reduce_now = tr && !reduced && b == tr->reduce_after_block && b + 1 < tr->restore_before_block && !last;
+    const bool restore_now = tr && reduced && b + 1 == tr->restore_before_block && !last;
+    const float* nmod = last ? nullptr : mods + (size_t)6 * d * (b + 1);
+    const bool emit_next = !last && !reduce_now && !restore_now;
+    const int vt_ld = (int)round_up((size_t)cur_n, 64);
+    H3_TRY(run_block_body(cfg, &w[b], mod, cur, cur_n, cur_rope, B, vt_ld,
+                          emit_next ? nmod : nullptr, emit_next ? nmod + d : nullptr, stream));
+    if (reduce_now) {
+      {
+        TimedLaunch tl(kReduce, stream);
+        h3::token_reduce_kernel<<<pg.n_red, h3::kRowThreads, 0, stream>>>(xfull, d, pg, xred, nullptr);
+        H3_CUDA(cudaGetLastError());
+      }
+      cur = xred;
+      cur_n = pg.n_red;
+      cur_rope = rope_red;
+      reduced = true;
+      H3_TRY(launch_rows(cur, nullptr, nullptr, nmod, nmod + d, B.base + ar.a2, cur_n, d, cfg->eps, stream));
+    } else if (restore_now) {
+      {
+        TimedLaunch tl(kReduce, stream);
+        h3::token_restore_kernel<<<pg.n_red, h3::kRowThreads, 0, stream>>>(xred, xfull, d, pg, xfull);
+        H3_CUDA(cudaGetLastError());
+      }
+      cur = xfull;
+      cur_n = n_tokens;
+      cur_rope = rope_full;
+      reduced = false;
+      H3_TRY(launch_rows(cur, nullptr, nullptr, nmod, nmod + d, B.base + ar.a2, cur_n, d, cfg->eps, stream));
+    }
+  }
+  if (reduced) {
+    TimedLaunch tl(kReduce, stream);
+    h3::token_restore_kernel<<<pg.n_red, h3::kRowThreads, 0, stream>>>(xred, xfull, d, pg, xfull);
+    H3_CUDA(cudaGetLastError());
+  }
+  return H3DIT_OK;
+}
+
+h3dit_status h3dit_quantize_act(const void* x_bf16, int rows, int cols, int group, int8_t* q, float* scales,
+                                cudaStream_t stream) {
+  if (!x_bf16 || !q || !scales) return fail(H3DIT_E_INVAL, "NULL pointer");
+  if (rows < 1 || cols < 1 || group < 1) return fail(H3DIT_E_INVAL, "non-positive shape");
+  if (cols % group != 0) return fail(H3DIT_E_INVAL, "group %d does not divide cols %d", group, cols);
+  if (group % 8 != 0) return fail(H3DIT_E_UNSUPPORTED, "group %d (multiple of 8)", group);
+  if (!aligned(x_bf16, 16) || !aligned(q, 8)) return fail(H3DIT_E_INVAL, "x must be 16-byte, q 8-byte aligned");
+  const long long blocks = 1LL * rows * (cols / group);
+  if (blocks > 0x7fffffffLL) return fail(H3DIT_E_UNSUPPORTED, "too many groups");
+  TimedLaunch tl(kQuant, stream);
+  h3::quantize_kernel<<<(unsigned)blocks, h3::kRowThreads, 0, stream>>>(static_cast<const bf16*>(x_bf16), cols, group, q,
+                                                                       scales);
+  H3_CUDA(cudaGetLastError());
+  return H3DIT_OK;
+}
+
+h3dit_status h3dit_quantize_weight(const void* w_bf16, int out, int in, int8_t* q, float* scales,
+                                   cudaStream_t stream) {
+  return h3dit_quantize_act(w_bf16, out, in, in, q, scales, stream);
+}
+
+int h3dit_reduced_tokens(int n_tokens, const h3dit_video_grid* g) {
+  if (!g || check_grid(g, n_tokens) != H3DIT_OK) return -1;
+  return pair_grid(g, n_tokens).n_red;
+}
+
+h3dit_status h3dit_token_reduce(const void* x_full, int n_tokens, int d, const h3dit_video_grid* grid, void* x_red,
+                                void* side, cudaStream_t stream) {
+  if (!x_full || !x_red) return fail(H3DIT_E_INVAL, "NULL pointer");
+  if (n_tokens < 1 || d < 8 || d % 8 != 0) return fail(H3DIT_E_INVAL, "shape %d x %d (d %% 8 == 0)", n_tokens, d);
+  H3_TRY(check_grid(grid, n_tokens));
+  if (!aligned(x_full, 16) || !aligned(x_red, 16) || (side && !aligned(side, 16)))
+    return fail(H3DIT_E_INVAL, "tensors must be 16-byte aligned");
+  const h3::PairGrid pg = pair_grid(grid, n_tokens);
+  TimedLaunch tl(kReduce, stream);
+  h3::token_reduce_kernel<<<pg.n_red, h3::kRowThreads, 0, stream>>>(static_cast<const bf16*>(x_full), d, pg,
+                                                                    static_cast<bf16*>(x_red), static_cast<bf16*>(side));
+  H3_CUDA(cudaGetLastError());
+  return H3DIT_OK;
+}
+
+h3dit_status h3dit_token_restore(const void* x_red, const void* side, int n_tokens, int d,
+                                 const h3dit_video_grid* grid, void* x_full, cudaStream_t stream) {
+  if (!x_red || !side || !x_full) return fail(H3DIT_E_INVAL, "NULL pointer");
+  if (n_tokens < 1 || d < 8 || d % 8 != 0) return fail(H3DIT_E_INVAL, "shape %d x %d (d %% 8 == 0)", n_tokens, d);
+  H3_TRY(check_grid(grid, n_tokens));
+  if (!aligned(x_full, 16) || !aligned(x_red, 16) || !aligned(side, 16))
+    return fail(H3DIT_E_INVAL, "tensors must be 16-byte aligned");
+  const h3::PairGrid pg = pair_grid(grid, n_tokens);
+  TimedLaunch tl(kReduce, stream);
+  h3::token_restore_kernel<<<pg.n_red, h3::kRowThreads, 0, stream>>>(
+      static_cast<const bf16*>(x_red), static_cast<const bf16*>(side), d, pg, static_cast<bf16*>(x_full));
+  H3_CUDA(cudaGetLastError());
+  return H3DIT_OK;
+}
+
+h3dit_status h3dit_reduced_positions(const float* pos, int n_tokens, const h3dit_video_grid* grid, float* pos_red,
+                                     cudaStream_t stream) {
+  if (!pos || !pos_red) return fail(H3DIT_E_INVAL, "NULL pointer");
+  if (n_tokens < 1) return fail(H3DIT_E_INVAL, "n_tokens %d", n_tokens);
+  H3_TRY(check_grid(grid, n_tokens));
+  const h3::PairGrid pg = pair_grid(grid, n_tokens);
+  TimedLaunch tl(kReduce, stream);
+  h3::reduced_positions_kernel<<<(pg.n_red + 127) / 128, 128, 0, stream>>>(pos, pg, pos_red);
+  H3_CUDA(cudaGetLastError());
+  return H3DIT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,291 @@
+// HBM-bound row kernels: AdaLN, the gated residual fused with the next AdaLN,
+// dynamic int8 quantisation, horizontal-pair token reduce/restore, and the
+// RoPE cos/sin table.  One CTA of 128 threads per row, 16-byte loads and
+// stores, warp-shuffle reductions; a row of up to 8192 BF16 stays in
+// registers between the residual, the statistics and the normalisation.
+#pragma once
+#include "ptx.cuh"
+
+namespace h3 {
+
+constexpr int kRowThreads = 128;
+constexpr int kRowMaxVec = 8;   // 8 x 128 threads x 8 values = 8192 columns
+
+__device__ __forceinline__ float block_sum_128(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5;
+  __syncthreads();   // red[] may still be read by a previous reduction
+  if ((threadIdx.x & 31) == 0) red[w] = v;
+  __syncthreads();
+  return red[0] + red[1] + red[2] + red[3];
+}
+
+__device__ __forceinline__ void unpack8(const uint4 u, float (&f)[8]) {
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __bfloat1622float2(b[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+
+// x_out = bf16(x + gate * branch) (if GATE) and h = bf16(LN(x_out)(1+scale)+shift)
+// (if NORM).  LN statistics in fp32 over the rounded row: mean, then the
+// biased variance of (x - mean) from the register copy.
+template <bool GATE, bool NORM>
+__global__ void __launch_bounds__(kRowThreads)
+    gate_adaln_kernel(__nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ branch,
+                      const float* __restrict__ gate, const float* __restrict__ shift,
+                      const float* __restrict__ scale, __nv_bfloat16* __restrict__ h, int d,
+                      float eps) {
+  __shared__ float red[4];
+  const size_t row = blockIdx.x;
+  const int nvec = d >> 3;
+  uint4* xr = reinterpret_cast<uint4*>(x + row * d);
+  const uint4* br = reinterpret_cast<const uint4*>(branch + (GATE ? row * d : 0));
+  float v[kRowMaxVec][8];
+  float sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRowMaxVec; ++i) {
+    const int idx = i * kRowThreads + threadIdx.x;
+    if (idx < nvec) {
+      unpack8(xr[idx], v[i]);
+      if (GATE) {
+        float b[8];
+        unpack8(br[idx], b);
+        const float4 g0 = __ldg(reinterpret_cast<const float4*>(gate) + 2 * idx);
+        const float4 g1 = __ldg(reinterpret_cast<const float4*>(gate) + 2 * idx + 1);
+        const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[i][e] = fmaf(g[e], b[e], v[i][e]);
+        const uint4 packed = pack8(v[i]);
+        xr[idx] = packed;
+        unpack8(packed, v[i]);   // continue with the rounded residual
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sum += v[i][e];
+    }
+  }
+  if (!NORM) return;
+  const float mean = block_sum_128(sum, red) / static_cast<float>(d);
+  float sq = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRowMaxVec; ++i) {
+    const int idx = i * kRowThreads + threadIdx.x;
+    if (idx < nvec) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float t = v[i][e] - mean;
+        sq = fmaf(t, t, sq);
+      }
+    }
+  }
+  const float var = block_sum_128(sq, red) / static_cast<float>(d);
+  const float rstd = rsqrtf(var + eps);
+  uint4* hr = reinterpret_cast<uint4*>(h + row * d);
+#pragma unroll
+  for (int i = 0; i < kRowMaxVec; ++i) {
+    const int idx = i * kRowThreads + threadIdx.x;
+    if (idx < nvec) {
+      const float4 s0 = __ldg(reinterpret_cast<const float4*>(scale) + 2 * idx);
+      const float4 s1 = __ldg(reinterpret_cast<const float4*>(scale) + 2 * idx + 1);
+      const float4 b0 = __ldg(reinterpret_cast<const float4*>(shift) + 2 * idx);
+      const float4 b1 = __ldg(reinterpret_cast<const float4*>(shift) + 2 * idx + 1);
+      const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+      const float sh[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+      float o[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = fmaf((v[i][e] - mean) * rstd, 1.f + sc[e], sh[e]);
+      hr[idx] = pack8(o);
+    }
+  }
+}
+
+// Symmetric absmax int8 quantisation of groups of `group` columns; one CTA
+// per (row, group).  s = absmax / 127 and x / s both correctly rounded fp32
+// divisions; round half to even; clamp to [-127, 127]; zero group -> 0.
+__global__ void __launch_bounds__(kRowThreads)
+    quantize_kernel(const __nv_bfloat16* __restrict__ x, int cols, int group, int8_t* __restrict__ q,
+                    float* __restrict__ scales) {
+  __shared__ float red[4];
+  const int groups = cols / group;
+  const size_t row = blockIdx.x / groups;
+  const int g = blockIdx.x - static_cast<int>(row) * groups;
+  const uint4* src = reinterpret_cast<const uint4*>(x + row * cols + static_cast<size_t>(g) * group);
+  const int nvec = group >> 3;
+  float amax = 0.f;
+  for (int idx = threadIdx.x; idx < nvec; idx += kRowThreads) {
+    float f[8];
+    unpack8(src[idx], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  const float s = __fdiv_rn(amax, 127.0f);
+  if (threadIdx.x == 0) scales[row * groups + g] = s;
+  uint2* dst = reinterpret_cast<uint2*>(q + row * cols + static_cast<size_t>(g) * group);
+  for (int idx = threadIdx.x; idx < nvec; idx += kRowThreads) {
+    float f[8];
+    unpack8(src[idx], f);
+    uint32_t w[2] = {0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      int c = 0;
+      if (s != 0.f) {
+        c = __float2int_rn(__fdiv_rn(f[e], s));
+        c = max(-127, min(127, c));
+      }
+      w[e >> 2] |= (static_cast<uint32_t>(c) & 0xFFu) << (8 * (e & 3));
+    }
+    dst[idx] = make_uint2(w[0], w[1]);
+  }
+}
+
+// Row maps of the horizontal-pair reduction.  Full row i -> reduced row.
+struct PairGrid {
+  int offset, T, Hh, W, Wr;   // Wr = ceil(W/2)
+  int n_full, n_red;
+};
+
+// Reduced row r -> first full row and member count (1 or 2).
+__device__ __forceinline__ void reduced_to_full(const PairGrid& g, int r, int& i0, int& cnt) {
+  const int nv_red = g.T * g.Hh * g.Wr;
+  if (r < g.offset) { i0 = r; cnt = 1; return; }
+  if (r < g.offset + nv_red) {
+    const int k = r - g.offset;
+    const int rowi = k / g.Wr;
+    const int j = k - rowi * g.Wr;
+    i0 = g.offset + rowi * g.W + 2 * j;
+    cnt = (2 * j + 1 < g.W) ? 2 : 1;
+    return;
+  }
+  i0 = r + (g.T * g.Hh * g.W - nv_red);
+  cnt = 1;
+}
+
+// One CTA per reduced row: mean of the pair (fp32, rounded to BF16), or a
+// copy; optionally also copies the members into `side`.
+__global__ void __launch_bounds__(kRowThreads)
+    token_reduce_kernel(const __nv_bfloat16* __restrict__ xf, int d, PairGrid g,
+                        __nv_bfloat16* __restrict__ xr, __nv_bfloat16* __restrict__ side) {
+  const int r = blockIdx.x;
+  int i0, cnt;
+  reduced_to_full(g, r, i0, cnt);
+  const uint4* a = reinterpret_cast<const uint4*>(xf + static_cast<size_t>(i0) * d);
+  const uint4* b = reinterpret_cast<const uint4*>(xf + static_cast<size_t>(i0 + (cnt - 1)) * d);
+  uint4* o = reinterpret_cast<uint4*>(xr + static_cast<size_t>(r) * d);
+  const int nvec = d >> 3;
+  for (int idx = threadIdx.x; idx < nvec; idx += kRowThreads) {
+    const uint4 ua = a[idx];
+    if (cnt == 2) {
+      const uint4 ub = b[idx];
+      float fa[8], fb[8], m[8];
+      unpack8(ua, fa);
+      unpack8(ub, fb);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) m[e] = (fa[e] + fb[e]) * 0.5f;
+      o[idx] = pack8(m);
+      if (side) {
+        reinterpret_cast<uint4*>(side + static_cast<size_t>(i0) * d)[idx] = ua;
+        reinterpret_cast<uint4*>(side + static_cast<size_t>(i0 + 1) * d)[idx] = ub;
+      }
+    } else {
+      o[idx] = ua;
+      if (side) reinterpret_cast<uint4*>(side + static_cast<size_t>(i0) * d)[idx] = ua;
+    }
+  }
+}
+
+// One CTA per reduced row: writes its one or two full rows.  A paired member
+// becomes side[i] + (x_red[p] - bf16(mean(side pair))) in fp32, rounded.
+// x_full may be the same buffer as side (each CTA reads its pair before
+// writing it).
+__global__ void __launch_bounds__(kRowThreads)
+    token_restore_kernel(const __nv_bfloat16* __restrict__ xr, const __nv_bfloat16* side, int d,
+                         PairGrid g, __nv_bfloat16* xf) {
+  const int r = blockIdx.x;
+  int i0, cnt;
+  reduced_to_full(g, r, i0, cnt);
+  const uint4* red = reinterpret_cast<const uint4*>(xr + static_cast<size_t>(r) * d);
+  const int nvec = d >> 3;
+  for (int idx = threadIdx.x; idx < nvec; idx += kRowThreads) {
+    const uint4 ur = red[idx];
+    if (cnt == 2) {
+      const uint4 ua = reinterpret_cast<const uint4*>(side + static_cast<size_t>(i0) * d)[idx];
+      const uint4 ub = reinterpret_cast<const uint4*>(side + static_cast<size_t>(i0 + 1) * d)[idx];
+      float fa[8], fb[8], fr[8], m[8], oa[8], ob[8];
+      unpack8(ua, fa);
+      unpack8(ub, fb);
+      unpack8(ur, fr);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) m[e] = (fa[e] + fb[e]) * 0.5f;
+      const uint4 um = pack8(m);   // the value the pair held when reduced
+      unpack8(um, m);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float upd = fr[e] - m[e];
+        oa[e] = fa[e] + upd;
+        ob[e] = fb[e] + upd;
+      }
+      reinterpret_cast<uint4*>(xf + static_cast<size_t>(i0) * d)[idx] = pack8(oa);
+      reinterpret_cast<uint4*>(xf + static_cast<size_t>(i0 + 1) * d)[idx] = pack8(ob);
+    } else {
+      reinterpret_cast<uint4*>(xf + static_cast<size_t>(i0) * d)[idx] = ur;
+    }
+  }
+}
+
+__global__ void reduced_positions_kernel(const float* __restrict__ pos, PairGrid g,
+                                         float* __restrict__ out) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= g.n_red) return;
+  int i0, cnt;
+  reduced_to_full(g, r, i0, cnt);
+#pragma unroll
+  for (int a = 0; a < 3; ++a) {
+    const float p0 = pos[static_cast<size_t>(i0) * 3 + a];
+    const float p1 = pos[static_cast<size_t>(i0 + cnt - 1) * 3 + a];
+    out[static_cast<size_t>(r) * 3 + a] = cnt == 2 ? (p0 + p1) * 0.5f : p0;
+  }
+}
+
+// cos/sin of pos[axis] * theta^(-2i/sec) for every (token, pair); pairs are
+// numbered across the head in section order (t, y, x).
+struct RopeSpec {
+  int head_dim;
+  int sec[3];
+  float theta;
+};
+
+__global__ void rope_table_kernel(const float* __restrict__ pos, int n, RopeSpec rs,
+                                  float2* __restrict__ table) {
+  const int half = rs.head_dim / 2;
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= n * half) return;
+  const int t = idx / half;
+  const int p = idx - t * half;
+  int axis = 0, start = 0;
+  while (axis < 2 && 2 * p >= start + rs.sec[axis]) {
+    start += rs.sec[axis];
+    ++axis;
+  }
+  const float i = static_cast<float>(p - start / 2);
+  const float omega = powf(rs.theta, -2.0f * i / static_cast<float>(rs.sec[axis]));
+  const float ang = pos[static_cast<size_t>(t) * 3 + axis] * omega;
+  float s, c;
+  sincosf(ang, &s, &c);
+  table[idx] = make_float2(c, s);
+}
+
+}  // namespace h3

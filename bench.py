@@ -1,0 +1,406 @@
+#!/usr/bin/env python3
+"""Benchmark of the MiniMax-H3 DiT block / 50-block denoiser step on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One JSON line on rank 0.  A "step" is one pass of the hot path over one batch
+of seeded synthetic input; the headline workload is one full-width BF16 DiT
+block at the 512x512x22-frame class (d 5120, 40 x 128 heads, MLP 20480,
+N 6912 = 6x32x32 video + 512 text + 256 audio) and `value` is its throughput
+in TFLOP/s (4 projections + 2 attention contractions per block).  The
+50-block step latency at the 864x480 class (N 10488) with and without token
+reduction is reported under "step".
+
+Multi-GPU: the block does not shard (one request per GPU); N GPUs run N
+independent replicas with no collective on the data path, launched by
+torchrun, barrier + max-over-ranks timing, `value` = all ranks' FLOPs / time.
+
+--impl reference times the fp64 CPU oracle (the deliberately slow
+correctness baseline) on the host cores on a bounded sample of the same
+workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "DiT block TFLOP/s (BF16/INT8) and 50-block step ms; % of tensor/HBM roofline"
+WORKLOAD_DESC = ("block_512: one BF16 MiniMax-H3 DiT block, d=5120, 40x128 heads, MLP 20480 GELU-tanh, "
+                 "N=6912 tokens (video 6x32x32 + 512 text + 256 audio), 3D RoPE, full attention")
+CPU_SAMPLE_TOKENS = 1024
+
+
+def block_flops(n, d, f):
+    return 2.0 * n * d * (3 * d) + 2.0 * n * d * d + 4.0 * n * d * f + 4.0 * n * n * d
+
+
+def gemm_flops(n, d, f):
+    return 2.0 * n * d * (3 * d) + 2.0 * n * d * d + 4.0 * n * d * f
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            j = json.load(fh)
+        return j.get("bf16_tflops", 1800.0), j.get("bf16_tflops_sustained", 1400.0), j.get("hbm_gbs", 6400.0), "measured"
+    return 1800.0, 1400.0, 6400.0, "fallback"
+
+
+def kernel_source_hash():
+    csrc = os.path.join(ROOT, "audio_diffusion_transformer_fwd_b300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu capture, if it was taken
+    on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        j = json.load(fh)
+    if j.get("source_hash") != kernel_source_hash():
+        return None
+    return j.get("kernels", {}).get(kernel_key)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# --------------------------------------------------------------------------- CPU oracle arm
+def oracle_sample_tflops(seconds_hint=False):
+    """Time the fp64 oracle block at the workload's widths on a bounded token
+    sample; returns (TFLOP/s, seconds, cores, sample description)."""
+    import numpy as np
+    import oracle as O
+    from audio_diffusion_transformer_fwd_b300 import synth
+    w = synth.WORKLOADS["block_512"]
+    n = CPU_SAMPLE_TOKENS
+    cfg = O.BlockConfig(d=w.d, heads=w.heads, head_dim=w.head_dim, ffn=w.ffn, eps=w.eps,
+                        rope_sections=w.sections, rope_theta=w.theta)
+    wt = synth.host_block_weights(w.d, w.ffn, seed=0)
+    mod = synth.host_mod(w.d, seed=0)
+    x = synth.host_activations(n, w.d, seed=0)
+    pos = synth.positions(w.video, w.n_text, w.n_audio)[:n]
+    t0 = time.perf_counter()
+    O.block_forward(x, wt, mod, pos, cfg)
+    dt = time.perf_counter() - t0
+    fl = block_flops(n, w.d, w.ffn)
+    cores = os.cpu_count()
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        cores = max((i.get("num_threads", 0) for i in info), default=cores) or cores
+    except Exception:
+        pass
+    desc = (f"fp64 numpy oracle, one block at d=5120/40x128/F=20480 over the first {n} of the 6912 tokens "
+            f"(attention over those {n}); {fl:.3e} FLOP")
+    return fl / dt / 1e12, dt, cores, desc
+
+
+def run_reference(args):
+    ws, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    vals = []
+    for _ in range(args.warmup):
+        oracle_sample_tflops()
+    t_all = 0.0
+    for _ in range(args.steps):
+        v, dt, cores, desc = oracle_sample_tflops()
+        vals.append(v)
+        t_all += dt
+    value = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * t_all / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD_DESC, "sample": f"{CPU_SAMPLE_TOKENS} tokens"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    from audio_diffusion_transformer_fwd_b300 import h3dit as H
+    from audio_diffusion_transformer_fwd_b300 import synth
+
+    ws, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(v):
+        if dist is None:
+            return v
+        t = torch.tensor([v], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return t.item()
+
+    burst, sustained, hbm, peak_src = measured_peaks()
+    w = synth.WORKLOADS["block_512"]
+    n, d, f = w.n_tokens, w.d, w.ffn
+    shape = H.BlockShape(w.d, w.heads, w.head_dim, w.ffn, w.eps, w.sections, w.theta)
+    stream = torch.cuda.current_stream()
+    wdev = synth.device_block_weights(d, f, seed=rank, block=0)
+    bw = H.block_weights(wdev["w_qkv"], wdev["w_o"], wdev["w1"], wdev["w2"])
+    mod = synth.device_mods(1, d, seed=rank)
+    x = synth.device_activations(n, d, seed=rank)
+    pos = torch.from_numpy(synth.positions(w.video, w.n_text, w.n_audio)).cuda()
+    nbytes = H.h3dit_workspace_size(shape, n)
+    wsb = torch.empty(nbytes, device="cuda", dtype=torch.uint8)
+
+    def step():
+        H.h3dit_block_forward(shape, bw, mod, x, pos, n, wsb, nbytes, stream)
+
+    for _ in range(args.warmup):
+        step()
+    H.h3dit_check_device_error(stream)
+
+    # ---- device-timed region (inputs resident; weights 629 MB > L2 per step)
+    sampler = ClockSampler(local)
+    sampler.start()
+    H.h3dit_timing_reset()
+    H.h3dit_timing_enable(True)
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    barrier()
+    H.h3dit_timing_enable(False)
+    clocks = sampler.stop()
+    H.h3dit_check_device_error(stream)
+    ms = max_over_ranks(ev0.elapsed_time(ev1)) / args.steps
+    per_class = {name: H.h3dit_timing_read(k) for name, k in
+                 (("rows", H.KC_ROWS), ("qkv", H.KC_QKV), ("attention", H.KC_ATTN), ("out_proj", H.KC_OPROJ),
+                  ("fc1", H.KC_FC1), ("fc2", H.KC_FC2))}
+    launches = sum(c for _, c in per_class.values())
+    fl = block_flops(n, d, f)
+    value = fl * ws / (ms * 1e-3) / 1e12
+
+    gemm_ms = sum(per_class[k][0] for k in ("qkv", "out_proj", "fc1", "fc2")) / args.steps
+    gemm_launch = sum(per_class[k][1] for k in ("qkv", "out_proj", "fc1", "fc2")) / args.steps
+    attn_ms = per_class["attention"][0] / args.steps
+    rows_ms = per_class["rows"][0] / args.steps
+    gfl = gemm_flops(n, d, f)
+    achieved = gfl / (gemm_ms * 1e-3) / 1e12
+    kernels = {
+        "qkv_gemm": {"ms": per_class["qkv"][0] / args.steps, "tflops": 2.0 * n * d * 3 * d / (per_class["qkv"][0] / args.steps * 1e-3) / 1e12},
+        "out_proj_gemm": {"ms": per_class["out_proj"][0] / args.steps, "tflops": 2.0 * n * d * d / (per_class["out_proj"][0] / args.steps * 1e-3) / 1e12},
+        "fc1_gemm": {"ms": per_class["fc1"][0] / args.steps, "tflops": 2.0 * n * d * f / (per_class["fc1"][0] / args.steps * 1e-3) / 1e12},
+        "fc2_gemm": {"ms": per_class["fc2"][0] / args.steps, "tflops": 2.0 * n * d * f / (per_class["fc2"][0] / args.steps * 1e-3) / 1e12},
+        "attention": {"ms": attn_ms, "tflops": 4.0 * n * n * d / (attn_ms * 1e-3) / 1e12,
+                      "frac_of_burst": 4.0 * n * n * d / (attn_ms * 1e-3) / 1e12 / burst},
+        "row_kernels": {"ms": rows_ms, "note": "rope table + AdaLN + 2 gated residual/AdaLN per block"},
+    }
+    # two gated-residual+AdaLN rows per block: read x, branch; write x, h (8 N d bytes each)
+    rows_gbs = None
+    if rows_ms > 0:
+        rows_gbs = (2 * 8.0 * n * d + 4.0 * n * d) / (rows_ms * 1e-3) / 1e9
+        kernels["row_kernels"]["gbs"] = rows_gbs
+        kernels["row_kernels"]["frac_of_hbm"] = rows_gbs / hbm
+
+    roofline = {"kernel": "tcgen05 BF16 GEMM (QKV+RoPE, out-proj, FC1+GELU, FC2), all launches of a block",
+                "bound": "tensor", "achieved": achieved, "peak": burst, "unit": "TFLOP/s",
+                "frac": achieved / burst, "peak_source": f"{peak_src} bf16 burst (cuBLAS 8192^3)",
+                "traffic": ncu_traffic("gemm_per_block"), "algorithmic_flops_per_block": gfl,
+                "launches_per_block": gemm_launch}
+
+    # ---- end-to-end through the C ABI with host buffers
+    xh = torch.empty((n, d), dtype=torch.bfloat16).pin_memory()
+    xh.copy_(x.cpu())
+    modh = mod.cpu().pin_memory()
+    posh = pos.cpu().pin_memory()
+    xo = torch.empty((n, d), dtype=torch.bfloat16).pin_memory()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(1, min(args.steps, 10))
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        x.copy_(xh, non_blocking=True)
+        mod.copy_(modh, non_blocking=True)
+        pos.copy_(posh, non_blocking=True)
+        step()
+        xo.copy_(x, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1)) / e2e_steps
+    h2d = xh.numel() * 2 + modh.numel() * 4 + posh.numel() * 4
+    d2h = xo.numel() * 2
+
+    # ---- 50-block steps (864x480 class), latency
+    step_res = {}
+    if not args.skip_step:
+        step_res = run_steps(args, H, synth, torch, stream, barrier, max_over_ranks, rank)
+
+    cpu = None
+    if rank == 0 and not args.skip_cpu:
+        v, dt, cores, desc = oracle_sample_tflops()
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc, "seconds": dt}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) weights, N(0,0.1) AdaLN, N(0,1) x)",
+            "config": {"workload": WORKLOAD_DESC, "parallelism": f"replicas x{ws}",
+                       "l2": "inputs larger than L2: 629 MB of block weights streamed every step"},
+            "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu,
+            "e2e": {"value": fl * ws / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": int(launches), "clocks": clocks, "step": step_res,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_steps(args, H, synth, torch, stream, barrier, max_over_ranks, rank):
+    """50-block step latency at the 864x480 class, without and with token
+    reduction (same weights)."""
+    w = synth.WORKLOADS["step_864"]
+    n, d, f, nb = w.n_tokens, w.d, w.ffn, w.n_blocks
+    shape = H.BlockShape(w.d, w.heads, w.head_dim, w.ffn, w.eps, w.sections, w.theta)
+    wdev = [synth.device_block_weights(d, f, seed=100 + rank, block=b) for b in range(nb)]
+    bws = [H.block_weights(t["w_qkv"], t["w_o"], t["w1"], t["w2"]) for t in wdev]
+    mods = synth.device_mods(nb, d, seed=100 + rank)
+    x0 = synth.device_activations(n, d, seed=100 + rank)
+    x = x0.clone()
+    pos = torch.from_numpy(synth.positions(w.video, w.n_text, w.n_audio)).cuda()
+    T, Hh, W = w.video
+    out = {}
+    _, sustained, _, _ = measured_peaks()
+    for name, tr in (("step_864", None),
+                     ("step_864_token_reduction", H.reduction(H.video_grid(0, T, Hh, W), 3, 40))):
+        nbytes = H.h3dit_workspace_size(shape, n, tr)
+        wsb = torch.empty(nbytes, device="cuda", dtype=torch.uint8)
+        reps = max(1, min(3, args.steps))
+        for _ in range(max(1, min(2, args.warmup))):
+            x.copy_(x0)
+            H.h3dit_step_forward(shape, bws, mods, x, pos, n, tr, wsb, nbytes, stream)
+        H.h3dit_check_device_error(stream)
+        barrier()
+        tot = 0.0
+        for _ in range(reps):
+            x.copy_(x0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            H.h3dit_step_forward(shape, bws, mods, x, pos, n, tr, wsb, nbytes, stream)
+            e1.record(stream)
+            barrier()
+            tot += e0.elapsed_time(e1)
+        ms = max_over_ranks(tot / reps)
+        if tr is None:
+            fl = nb * block_flops(n, d, f)
+        else:
+            nr = H.h3dit_reduced_tokens(n, H.video_grid(0, T, Hh, W))
+            fl = 4 * block_flops(n, d, f) + 36 * block_flops(nr, d, f) + 10 * block_flops(n, d, f)
+        out[name] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12, "frac_of_sustained": fl / (ms * 1e-3) / 1e12 / sustained,
+                     "n_tokens": n, "blocks": nb, "reps": reps}
+        del wsb
+    del wdev
+    torch.cuda.empty_cache()
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--skip-step", action="store_true", help="omit the 50-block step latencies")
+    ap.add_argument("--skip-cpu", action="store_true", help="omit the oracle CPU baseline")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,284 @@
+/*
+ * h3dit.h - C ABI of the B300 (sm_103a) forward pass of the MiniMax-H3 DiT
+ * block and of the 50-block denoiser step.
+ *
+ * The method is described by web pages about h3.c ("h3-metal"), an Apple
+ * inference engine for MiniMax-H3:
+ *   [alphalab]  "h3-metal 把 MiniMax-H3 搬上 Apple Silicon：突破與代價（2026）",
+ *               model facts (33B dense single-stream Omni Transformer, 50 layers,
+ *               full attention) and the author's test table (warm 50-block forward).
+ *   [linlog]    linlog.top article 1265 on h3.c; sections "MiniMax H3：原生音频视频
+ *               一体化生成" (AdaLN branch precomputed at inference), "h3.c 的核心设计"
+ *               (QKV routed head-major), "int8 量化：从 36 秒到 19 秒" (dynamic int8),
+ *               "DiT 融合内核：减少全局内存往返" (gated AdaLN fusion, arena aliasing),
+ *               "Token 缩减：28% 的去噪时间消减" (horizontal-pair token reduction).
+ *   [steinslab] "零 Python 依赖：Redis 作者的 3.5 秒端侧实验", section "极简主控逻辑"
+ *               (spatial RoPE over t/h/w).
+ *
+ * Conventions for every entry point:
+ *  - Every pointer argument named as device memory is a device pointer owned
+ *    by the caller; the library never frees or keeps it past the call.  Host
+ *    pointers (configs, weight tables, grids) are read during the call only.
+ *  - BF16 tensors are row-major and token-major unless stated: [N][d] means
+ *    row t (a token) is d consecutive bfloat16 values.  Weights are [out][in]
+ *    (one row per output channel), the layout of a PyTorch Linear weight.
+ *  - Work is enqueued asynchronously on the given cudaStream_t (0 = legacy
+ *    default stream); nothing is synchronised except where stated.
+ *  - No entry point allocates device memory on the hot path; scratch comes
+ *    from the caller's workspace (h3dit_workspace_size).
+ *  - Every call returns an h3dit_status.  On failure nothing is enqueued
+ *    (argument errors) or the CUDA error is reported (launch errors), and
+ *    h3dit_last_error() returns a message for the calling thread.  The
+ *    library never prints, exits or aborts.
+ *  - Device-side waits are bounded: a kernel whose pipeline wait runs out
+ *    sets a device error word and returns; h3dit_check_device_error() reads
+ *    it and reports H3DIT_E_TIMEOUT.
+ */
+#ifndef H3DIT_H
+#define H3DIT_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define H3DIT_VERSION 1
+
+typedef enum {
+  H3DIT_OK = 0,
+  H3DIT_E_INVAL = 1,        /* a null pointer, a negative size, inconsistent shapes */
+  H3DIT_E_UNSUPPORTED = 2,  /* a shape this build does not implement (see each call) */
+  H3DIT_E_NOMEM = 3,        /* the workspace passed in is smaller than required */
+  H3DIT_E_CUDA = 4,         /* a CUDA runtime or driver call failed */
+  H3DIT_E_TIMEOUT = 5       /* a kernel's bounded pipeline wait ran out */
+} h3dit_status;
+
+typedef enum { H3DIT_BF16 = 0, H3DIT_INT8 = 1 } h3dit_precision;
+
+/* Shape of one block.  The pages give none of these numbers.
+ *  d            model width; a multiple of 256, at most 8192
+ *  heads        attention heads; heads * head_dim == d
+ *  head_dim     64 or 128
+ *  ffn          MLP width F; a multiple of 256
+ *  eps          LayerNorm epsilon (LayerNorm: biased variance, no affine)
+ *  rope_sections head-dim widths of the (t, y, x) RoPE sections; even, sum head_dim
+ *  rope_theta   RoPE base; pair i of a section of width s turns by pos * theta^(-2i/s)
+ *  precision    H3DIT_BF16 or H3DIT_INT8 (dynamic-int8 projections) */
+typedef struct {
+  int d;
+  int heads;
+  int head_dim;
+  int ffn;
+  float eps;
+  int rope_sections[3];
+  float rope_theta;
+  int precision;
+} h3dit_config;
+
+/* One block's projection weights, device pointers.
+ * BF16 precision: BF16 [out][in] matrices, scale pointers unused (may be NULL).
+ * INT8 precision: int8 codes [out][in] and fp32 per-output-channel scales
+ *   (h3dit_quantize_weight), as in [linlog] "int8 量化" (per-output-channel
+ *   weight scales).
+ *   w_qkv [3d][d]  rows 0..d-1 give Q (head h = rows h*Dh..), d..2d-1 K, 2d..3d-1 V
+ *   w_o   [d][d]   attention output projection
+ *   w1    [F][d]   MLP FC1
+ *   w2    [d][F]   MLP FC2 */
+typedef struct {
+  const void* w_qkv;
+  const void* w_o;
+  const void* w1;
+  const void* w2;
+  const float* s_qkv;
+  const float* s_o;
+  const float* s1;
+  const float* s2;
+} h3dit_block_weights;
+
+/* Target-video tokens: T*Hh*W consecutive rows starting at row `offset`,
+ * ordered t-major, then y, then x.  Other rows (text, audio, conditions)
+ * are never reduced. */
+typedef struct {
+  int offset;
+  int T;
+  int Hh;
+  int W;
+} h3dit_video_grid;
+
+/* Token-reduction schedule of the step ([linlog] "Token 缩减"): the video
+ * is paired after block reduce_after_block (0-based) and restored before
+ * block restore_before_block.  pos_reduced: device [N_reduced][3] fp32
+ * positions of the reduced sequence, or NULL to use the pair-mean positions
+ * (h3dit_reduced_positions). */
+typedef struct {
+  h3dit_video_grid grid;
+  int reduce_after_block;
+  int restore_before_block;
+  const float* pos_reduced;
+} h3dit_reduction;
+
+/* ---------------------------------------------------------------- housekeeping */
+
+/* Message of the last failed call on this thread ("" if none).  The string
+ * stays valid until the next call on this thread. */
+const char* h3dit_last_error(void);
+
+/* H3DIT_VERSION of the loaded library. */
+int h3dit_version(void);
+
+/* Synchronises `stream`, then reads and clears the device error word set by
+ * a kernel whose bounded wait ran out.  H3DIT_OK if clear, H3DIT_E_TIMEOUT
+ * if set, H3DIT_E_CUDA if the synchronisation itself failed. */
+h3dit_status h3dit_check_device_error(cudaStream_t stream);
+
+/* Per-kernel-class timing with CUDA events recorded on the launch stream
+ * around every launch while enabled (off by default).  Classes:
+ * 0 row kernels, 1 QKV GEMM, 2 attention, 3 out-projection GEMM, 4 FC1 GEMM,
+ * 5 FC2 GEMM, 6 token reduce/restore, 7 quantise.  h3dit_timing_read
+ * synchronises the recorded events and returns the total milliseconds and
+ * launch count of a class since the last reset. */
+h3dit_status h3dit_timing_enable(int on);
+h3dit_status h3dit_timing_reset(void);
+h3dit_status h3dit_timing_read(int kernel_class, double* total_ms, long long* launches);
+
+/* ---------------------------------------------------------------- the block and the step */
+
+/* Bytes of device workspace a block or step at n_tokens needs (tr may be
+ * NULL; with a reduction the reduced stream's buffers are included). */
+h3dit_status h3dit_workspace_size(const h3dit_config* cfg, int n_tokens,
+                                  const h3dit_reduction* tr, size_t* bytes);
+
+/* One dense single-stream DiT block, in place on x ([alphalab] model facts;
+ * [linlog] "DiT 融合内核"):
+ *   h  = LN(x) * (1 + scale1) + shift1
+ *   q, k, v = h W_qkv^T, heads split, q and k turned by 3D RoPE at `pos`
+ *   o  = softmax(q k^T / sqrt(Dh)) v over all tokens (non-causal, no mask)
+ *   x1 = x + gate1 * (o W_o^T)            rounded to BF16 and stored
+ *   h2 = LN(x1) * (1 + scale2) + shift2   (fused with the residual)
+ *   x  = x1 + gate2 * (GELU_tanh(h2 W1^T) W2^T)
+ * mod: device fp32 [6][d] = shift1, scale1, gate1, shift2, scale2, gate2
+ *      (the precomputed AdaLN branch, [linlog] "MiniMax H3" section).
+ * x:   device BF16 [n_tokens][d], read and overwritten.
+ * pos: device fp32 [n_tokens][3] (t, y, x) rotary positions.
+ * ws:  device workspace of at least h3dit_workspace_size bytes, 256-byte aligned.
+ * Errors: E_INVAL (nulls, n_tokens < 1), E_UNSUPPORTED (shape outside the
+ * limits of h3dit_config), E_NOMEM (ws_bytes too small), E_CUDA. */
+h3dit_status h3dit_block_forward(const h3dit_config* cfg, const h3dit_block_weights* w,
+                                 const float* mod, void* x, const float* pos, int n_tokens,
+                                 void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* The denoiser step: blocks 0..n_blocks-1 in order, block b with w[b] (a host
+ * array of n_blocks weight tables) and mods + 6*d*b, in place on x
+ * ([alphalab] 50 layers; [linlog] "--layers" trimming is n_blocks).  The
+ * gated residual of each block also emits the next block's AdaLN input
+ * ([linlog] "DiT 融合内核"), except at token-reduction boundaries.
+ * tr: NULL for no reduction, else the schedule above; x keeps the full
+ * resolution state while the reduced blocks run on a workspace copy.
+ * Errors as h3dit_block_forward; E_INVAL also for a grid outside the rows. */
+h3dit_status h3dit_step_forward(const h3dit_config* cfg, const h3dit_block_weights* w,
+                                int n_blocks, const float* mods, void* x, const float* pos,
+                                int n_tokens, const h3dit_reduction* tr, void* ws,
+                                size_t ws_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------- quantisation */
+
+/* Dynamic symmetric int8 quantisation ([linlog] "int8 量化": activations
+ * quantised dynamically; FC2 input with one scale per 1024 channels).
+ * For each row and each group of `group` consecutive columns:
+ *   s = absmax / 127 (fp32, correctly rounded); q = clamp(rne(x / s), -127, 127)
+ * with x / s correctly rounded in fp32 and ties to even; an all-zero group
+ * gives s = 0 and q = 0.
+ * x_bf16: device BF16 [rows][cols]; q: device int8 [rows][cols];
+ * scales: device fp32 [rows][cols / group].  group divides cols; cols % 8 == 0. */
+h3dit_status h3dit_quantize_act(const void* x_bf16, int rows, int cols, int group,
+                                int8_t* q, float* scales, cudaStream_t stream);
+
+/* Per-output-channel int8 weights ([linlog] "int8 量化"): the rule of
+ * h3dit_quantize_act with one group per row of w [out][in]. */
+h3dit_status h3dit_quantize_weight(const void* w_bf16, int out, int in, int8_t* q,
+                                   float* scales, cudaStream_t stream);
+
+/* ---------------------------------------------------------------- token reduction */
+
+/* Rows left after pairing: n_tokens - T*Hh*floor(W/2). */
+int h3dit_reduced_tokens(int n_tokens, const h3dit_video_grid* grid);
+
+/* Horizontal-pair reduction ([linlog] "Token 缩减"): video columns (2j, 2j+1)
+ * of every (t, y) row become their mean (fp32, rounded to BF16); an odd last
+ * column and every non-video row are copied.  x_full: device BF16
+ * [n_tokens][d]; x_red: device BF16 [h3dit_reduced_tokens][d]; side: device
+ * BF16 [n_tokens][d] copy of x_full, or NULL when the caller keeps x_full
+ * itself as the side state.  d % 8 == 0. */
+h3dit_status h3dit_token_reduce(const void* x_full, int n_tokens, int d,
+                                const h3dit_video_grid* grid, void* x_red, void* side,
+                                cudaStream_t stream);
+
+/* Restore ([linlog] "Token 缩减": each token returns its original value plus
+ * its pair's learned update): a paired token i of pair p becomes
+ *   side[i] + (x_red[p] - bf16(mean(side[2j], side[2j+1])))
+ * computed in fp32 and rounded to BF16; every other row takes x_red's row.
+ * With a zero update this is the identity, bit for bit.  x_full may alias side. */
+h3dit_status h3dit_token_restore(const void* x_red, const void* side, int n_tokens, int d,
+                                 const h3dit_video_grid* grid, void* x_full,
+                                 cudaStream_t stream);
+
+/* Pair-mean positions of the reduced sequence: device fp32 [n_tokens][3] ->
+ * [h3dit_reduced_tokens][3]. */
+h3dit_status h3dit_reduced_positions(const float* pos, int n_tokens,
+                                     const h3dit_video_grid* grid, float* pos_red,
+                                     cudaStream_t stream);
+
+/* ---------------------------------------------------------------- the block's steps one by one */
+
+/* AdaLN: h = bf16(LN(x) * (1 + scale) + shift), LayerNorm with biased
+ * variance over d, fp32 arithmetic.  x, h: device BF16 [n][d]; shift, scale:
+ * device fp32 [d]. */
+h3dit_status h3dit_adaln(const h3dit_config* cfg, const void* x, const float* shift,
+                         const float* scale, int n_tokens, void* h, cudaStream_t stream);
+
+/* Gated residual fused with the following AdaLN ([linlog] "DiT 融合内核",
+ * gated AdaLN fusion):  x = bf16(x + gate * branch) is written exactly and the
+ * rounded row is normalised: h = bf16(LN(x) * (1 + scale) + shift).
+ * shift/scale NULL: residual only (h unused).  Env H3DIT_DISABLE_GATED_ADALN=1
+ * runs the two halves as separate kernels (bit-identical results).
+ * x: device BF16 [n][d] in/out; branch: BF16 [n][d]; gate, shift, scale: fp32 [d]. */
+h3dit_status h3dit_gate_residual_adaln(const h3dit_config* cfg, void* x, const void* branch,
+                                       const float* gate, const float* shift,
+                                       const float* scale, int n_tokens, void* h,
+                                       cudaStream_t stream);
+
+/* RoPE table: cos/sin of every (token, pair) angle, device fp32
+ * [n_tokens][head_dim/2][2] (cos, sin), from device fp32 pos [n_tokens][3]. */
+h3dit_status h3dit_rope_table(const h3dit_config* cfg, const float* pos, int n_tokens,
+                              float* table, cudaStream_t stream);
+
+/* QKV projection with 3D RoPE in the epilogue and head-major outputs
+ * ([linlog] "h3.c 的核心设计": Q/K/V routed head-major for attention):
+ *   q[h][t][:] = RoPE(h_t . W_q[h]),  k likewise,  vt[h][c][t] = (h_t . W_v[h])_c
+ * h: BF16 [n][d]; w_qkv: BF16 [3d][d]; table: from h3dit_rope_table;
+ * q, k: BF16 [heads][n][head_dim]; vt: BF16 [heads][head_dim][vt_ld],
+ * vt_ld >= n, vt_ld % 8 == 0.  BF16 precision only. */
+h3dit_status h3dit_qkv_project(const h3dit_config* cfg, const void* h, const void* w_qkv,
+                               const float* table, int n_tokens, void* q, void* k, void* vt,
+                               int vt_ld, cudaStream_t stream);
+
+/* Full non-causal attention per head ([alphalab] full attention):
+ *   o[t][h*Dh + c] = sum_j softmax_j(q[h][t] . k[h][j] / sqrt(Dh)) vt[h][c][j]
+ * q, k: BF16 [heads][n][Dh]; vt: BF16 [heads][Dh][vt_ld]; o: BF16 [n][d]. */
+h3dit_status h3dit_attention(const h3dit_config* cfg, const void* q, const void* k,
+                             const void* vt, int vt_ld, int n_tokens, void* o,
+                             cudaStream_t stream);
+
+/* Projection c = act(a b^T): a BF16 [m][k], b BF16 [n][k] (a Linear weight),
+ * c BF16 [m][n]; act 0 = none, 1 = GELU tanh form.  n % 256 == 0,
+ * k % 64 == 0, any m >= 1. */
+h3dit_status h3dit_linear(const void* a, const void* b, int m, int n, int k, int act, void* c,
+                          cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* H3DIT_H */

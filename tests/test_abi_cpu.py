@@ -1,0 +1,67 @@
+"""The C-ABI library loads without a GPU and exports every entry point that
+include/h3dit.h declares; the Python binding names each of them.  No compute
+call is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from audio_diffusion_transformer_fwd_b300 import build as B
+from audio_diffusion_transformer_fwd_b300 import h3dit as H
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "h3dit.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(h3dit_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return ctypes.CDLL(B.LIB)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    syms = declared_symbols()
+    assert len(syms) >= 20
+    for s in syms:
+        assert hasattr(lib, s), f"{s} declared in h3dit.h but not exported"
+
+
+def test_binding_covers_the_header():
+    assert sorted(H._EXPORTS) == declared_symbols()
+
+
+def test_host_only_calls(lib):
+    lib.h3dit_version.restype = ctypes.c_int
+    assert lib.h3dit_version() == 1
+    g = H.video_grid(0, 6, 30, 54)
+    assert H.lib().h3dit_reduced_tokens(10488, ctypes.byref(g)) == 5628
+    bad = H.video_grid(0, 6, 30, 54)
+    assert H.lib().h3dit_reduced_tokens(100, ctypes.byref(bad)) == -1
+    shape = H.BlockShape(5120, 40, 128, 20480)
+    n1 = H.h3dit_workspace_size(shape, 6912)
+    n2 = H.h3dit_workspace_size(shape, 10488)
+    n3 = H.h3dit_workspace_size(shape, 10488, H.reduction(g, 3, 40))
+    assert 0 < n1 < n2 < n3
+    with pytest.raises(H.H3DitError) as e:
+        H.h3dit_workspace_size(H.BlockShape(5120, 40, 96, 20480), 10)
+    assert e.value.status == H.E_INVAL
+    with pytest.raises(H.H3DitError) as e:
+        H.h3dit_workspace_size(H.BlockShape(5120, 80, 64, 20000), 10)
+    assert e.value.status == H.E_UNSUPPORTED
+    assert "ffn" in H.lib().h3dit_last_error().decode()
+
+
+def test_workspace_aliasing_saves_memory():
+    """Arena aliasing keeps the block's activations to roughly
+    max(3Nd + V^T padding, NF) + 2Nd BF16 values plus the RoPE table."""
+    shape = H.BlockShape(5120, 40, 128, 20480)
+    n = 10488
+    got = H.h3dit_workspace_size(shape, n)
+    unaliased = 2 * n * (5120 * (1 + 3 + 1 + 1 + 1 + 1) + 20480)   # h, qkv, o, a, h2, m, u
+    assert got < 0.8 * unaliased
