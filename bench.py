@@ -139,55 +139,66 @@ def dist_setup():
 
 
 # --------------------------------------------------------------------------- CPU oracle arm
-def oracle_sample_tflops(seconds_hint=False):
-    """Time the fp64 oracle block at the workload's widths on a bounded token
-    sample; returns (TFLOP/s, seconds, cores, sample description)."""
-    import numpy as np
-    import oracle as O
-    from audio_diffusion_transformer_fwd_b300 import synth
-    w = synth.WORKLOADS["block_512"]
-    n = CPU_SAMPLE_TOKENS
-    cfg = O.BlockConfig(d=w.d, heads=w.heads, head_dim=w.head_dim, ffn=w.ffn, eps=w.eps,
-                        rope_sections=w.sections, rope_theta=w.theta)
-    wt = synth.host_block_weights(w.d, w.ffn, seed=0)
-    mod = synth.host_mod(w.d, seed=0)
-    x = synth.host_activations(n, w.d, seed=0)
-    pos = synth.positions(w.video, w.n_text, w.n_audio)[:n]
-    t0 = time.perf_counter()
-    O.block_forward(x, wt, mod, pos, cfg)
-    dt = time.perf_counter() - t0
-    fl = block_flops(n, w.d, w.ffn)
-    cores = os.cpu_count()
-    try:
-        import threadpoolctl
-        info = threadpoolctl.threadpool_info()
-        cores = max((i.get("num_threads", 0) for i in info), default=cores) or cores
-    except Exception:
-        pass
-    desc = (f"fp64 numpy oracle, one block at d=5120/40x128/F=20480 over the first {n} of the 6912 tokens "
-            f"(attention over those {n}); {fl:.3e} FLOP")
-    return fl / dt / 1e12, dt, cores, desc
+class OracleSample:
+    """The fp64 oracle block at the workload's widths (d 5120, 40 x 128 heads,
+    F 20480) over a bounded prefix of the workload's tokens; weights drawn
+    once.  Attention runs over the sampled tokens only."""
+
+    def __init__(self):
+        import oracle as O
+        from audio_diffusion_transformer_fwd_b300 import synth
+        self.O = O
+        self.w = w = synth.WORKLOADS["block_512"]
+        self.cfg = O.BlockConfig(d=w.d, heads=w.heads, head_dim=w.head_dim, ffn=w.ffn, eps=w.eps,
+                                 rope_sections=w.sections, rope_theta=w.theta)
+        self.wt = synth.host_block_weights(w.d, w.ffn, seed=0)
+        self.mod = synth.host_mod(w.d, seed=0)
+        self.x = synth.host_activations(w.n_tokens, w.d, seed=0)
+        self.pos = synth.positions(w.video, w.n_text, w.n_audio)
+        self.cores = os.cpu_count()
+        try:
+            import threadpoolctl
+            info = threadpoolctl.threadpool_info()
+            self.cores = max((i.get("num_threads", 0) for i in info), default=self.cores) or self.cores
+        except Exception:
+            pass
+
+    def run(self, n):
+        t0 = time.perf_counter()
+        self.O.block_forward(self.x[:n], self.wt, self.mod, self.pos[:n], self.cfg)
+        dt = time.perf_counter() - t0
+        return block_flops(n, self.w.d, self.w.ffn), dt
+
+    def desc(self, n):
+        return (f"fp64 numpy oracle: one block at d=5120, 40x128 heads, F=20480 over the first {n} of the "
+                f"6912 tokens (attention over those {n}), {block_flops(n, self.w.d, self.w.ffn):.3e} FLOP per step")
 
 
 def run_reference(args):
     ws, rank, _ = dist_setup()
     if rank != 0:
         return 0
-    vals = []
+    sample = OracleSample()
+    # size the per-step sample so that warm-up + timed steps take ~2.5 minutes
+    fl, dt = sample.run(256)
+    per_token_s = dt / 256
+    n = int(150.0 / max(1, args.steps + args.warmup) / per_token_s) // 64 * 64
+    n = max(64, min(CPU_SAMPLE_TOKENS, n))
     for _ in range(args.warmup):
-        oracle_sample_tflops()
-    t_all = 0.0
+        sample.run(n)
+    tot_fl, tot_s = 0.0, 0.0
     for _ in range(args.steps):
-        v, dt, cores, desc = oracle_sample_tflops()
-        vals.append(v)
-        t_all += dt
-    value = statistics.mean(vals)
+        fl, dt = sample.run(n)
+        tot_fl += fl
+        tot_s += dt
+    value = tot_fl / tot_s / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * t_all / max(1, args.steps),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * tot_s / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": WORKLOAD_DESC, "sample": f"{CPU_SAMPLE_TOKENS} tokens"},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
+        "data": "synthetic", "config": {"workload": WORKLOAD_DESC, "sample_tokens": n},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": sample.cores, "kind": "oracle",
+                         "sample": sample.desc(n)},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -319,8 +330,10 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and not args.skip_cpu:
-        v, dt, cores, desc = oracle_sample_tflops()
-        cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc, "seconds": dt}
+        sample = OracleSample()
+        fl_c, dt_c = sample.run(CPU_SAMPLE_TOKENS)
+        cpu = {"value": fl_c / dt_c / 1e12, "unit": "TFLOP/s", "cores": sample.cores, "kind": "oracle",
+               "sample": sample.desc(CPU_SAMPLE_TOKENS), "seconds": dt_c}
 
     if rank == 0:
         line = {
@@ -391,7 +404,7 @@ def run_steps(args, H, synth, torch, stream, barrier, max_over_ranks, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-step", action="store_true", help="omit the 50-block step latencies")

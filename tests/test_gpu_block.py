@@ -1,10 +1,16 @@
 """Block and step parity on the GPU through the C ABI against the fp64 oracle.
 
 Acceptance for the BF16 block: relative L2 <= 1e-2 and max-abs <= 5e-2 on the
-block output.  Because the output is dominated by the untouched residual,
-the branch (x_out - x_in) is also held to relative L2 <= 2e-2 against the
-oracle's branch, which a wrong projection or attention would fail by
+block output against the oracle evaluated in fp64 with the tensors the
+kernels store (h, q, k, v, o, a, x1, h2, u, m, x2) rounded to BF16.  Because
+the output is dominated by the residual, the branch (x_out - x_in) is also
+held to relative L2 <= 2e-2, which a wrong projection or attention fails by
 orders of magnitude.
+
+Against the pure fp64 oracle (no storage rounding) the bound is derived from
+the arithmetic: the residual is rounded to BF16 twice per block (x1 and x2),
+each time by at most 2^-8 of its magnitude, so max-abs <= 2^-7 * max|x| plus
+the 5e-2 branch allowance, and relative L2 <= 1e-2.
 """
 import numpy as np
 import pytest
@@ -36,10 +42,17 @@ def _run_block(w, x, wt, mod, pos, n):
     return host(xd)
 
 
-def _assert_block(got, ref, x):
-    r, m = rel_l2(got, ref), max_abs(got, ref)
-    rb = rel_l2(got - x, ref - x)
-    assert r <= 1e-2 and m <= 5e-2 and rb <= 2e-2, f"rel_l2={r:.2e} max_abs={m:.2e} branch_rel_l2={rb:.2e}"
+def assert_block(got, x, ref64, ref_bf):
+    r, m = rel_l2(got, ref_bf), max_abs(got, ref_bf)
+    rb = rel_l2(got - x, ref_bf - x)
+    # one BF16 step of the largest output, where a rounding lands on the
+    # other side of a tie (only matters once |x| >= 8)
+    mb = max(5e-2, 2.0 ** -7 * float(np.max(np.abs(ref_bf))))
+    assert r <= 1e-2 and m <= mb and rb <= 2e-2, \
+        f"vs BF16-storage oracle: rel_l2={r:.2e} max_abs={m:.2e} (<= {mb:.2e}) branch_rel_l2={rb:.2e}"
+    r64, m64 = rel_l2(got, ref64), max_abs(got, ref64)
+    bound = 2.0 ** -7 * float(np.max(np.abs(ref64))) + 5e-2
+    assert r64 <= 1e-2 and m64 <= bound, f"vs fp64 oracle: rel_l2={r64:.2e} max_abs={m64:.2e} (<= {bound:.2e})"
 
 
 @pytest.mark.parametrize("n", [256, 77, 1, 129])
@@ -51,7 +64,8 @@ def test_block_tiny(n):
     mod = synth.host_mod(w.d, seed=0)
     got = _run_block(w, x, wt, mod, pos, n)
     ref = O.block_forward(x, wt, mod, pos, oracle_cfg(w))
-    _assert_block(got, ref, x)
+    ref_bf = O.block_forward(x, wt, mod, pos, oracle_cfg(w), bf16_storage=True)
+    assert_block(got, x, ref, ref_bf)
 
 
 def test_block_tiny_strong_gates():
@@ -64,7 +78,8 @@ def test_block_tiny_strong_gates():
     mod = synth.host_mod(w.d, seed=2, std=1.0)
     got = _run_block(w, x, wt, mod, pos, n)
     ref = O.block_forward(x, wt, mod, pos, oracle_cfg(w))
-    _assert_block(got, ref, x)
+    ref_bf = O.block_forward(x, wt, mod, pos, oracle_cfg(w), bf16_storage=True)
+    assert_block(got, x, ref, ref_bf)
 
 
 def test_block_zero_gates_is_identity_bit_exact():

@@ -20,6 +20,7 @@ import oracle as O
 from audio_diffusion_transformer_fwd_b300 import h3dit as H
 from audio_diffusion_transformer_fwd_b300 import synth
 from tests.gpu_util import dev_f32, host, max_abs, oracle_cfg, rel_l2, shape_of
+from tests.test_gpu_block import assert_block
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -30,12 +31,6 @@ def _host_w(dev):
 
 def _bw(dev):
     return H.block_weights(dev["w_qkv"], dev["w_o"], dev["w1"], dev["w2"])
-
-
-def _check_rows(got_rows, ref_rows, x_rows):
-    r, m = rel_l2(got_rows, ref_rows), max_abs(got_rows, ref_rows)
-    rb = rel_l2(got_rows - x_rows, ref_rows - x_rows)
-    assert r <= 1e-2 and m <= 5e-2 and rb <= 2e-2, f"rel_l2={r:.2e} max_abs={m:.2e} branch={rb:.2e}"
 
 
 def test_block_512_sampled_rows():
@@ -53,8 +48,10 @@ def test_block_512_sampled_rows():
     H.h3dit_check_device_error()
     got = host(x)
     rows = [0, 127, 128, 1000, 4095, 6143, 6144, 6500, 6655, 6656, 6911]
-    ref = O.block_forward(x_in, _host_w(dev), host(mods[0]), pos, oracle_cfg(w), rows=rows)
-    _check_rows(got[rows], ref, x_in[rows])
+    wh, mh, cfg = _host_w(dev), host(mods[0]), oracle_cfg(w)
+    ref = O.block_forward(x_in, wh, mh, pos, cfg, rows=rows)
+    ref_bf = O.block_forward(x_in, wh, mh, pos, cfg, rows=rows, bf16_storage=True)
+    assert_block(got[rows], x_in[rows], ref, ref_bf)
 
 
 @pytest.mark.parametrize("reduce", [False, True])
@@ -88,23 +85,28 @@ def test_step_864_single_live_block(reduce):
     if not reduce:
         rows = [0, 5000, 9719, 9720, 10487]
         ref = O.block_forward(x_in, wl, ml, pos, cfg, rows=rows)
-        _check_rows(got[rows], ref, x_in[rows])
+        ref_bf = O.block_forward(x_in, wl, ml, pos, cfg, rows=rows, bf16_storage=True)
+        assert_block(got[rows], x_in[rows], ref, ref_bf)
     else:
         g = O.VideoGrid(0, T, Hh, W)
-        x_red, side = O.token_reduce(x_in, g)
         pos_red = O.reduced_positions(pos, g)
         # reduced rows: two video pairs and text/audio rows
         prow = [0, 2000, 4859, 4860, 5627]
-        y = O.block_forward(x_red, wl, ml, pos_red, cfg, rows=prow)
-        full_rows, ref_rows = [], []
-        for p, yp in zip(prow, y):
-            if p < T * Hh * ((W + 1) // 2):
-                i0 = (p // ((W + 1) // 2)) * W + 2 * (p % ((W + 1) // 2))
-                for i in (i0, i0 + 1):
+        refs = []
+        for storage in (False, True):
+            x_red, _ = O.token_reduce(x_in, g, bf16_storage=storage)
+            y = O.block_forward(x_red, wl, ml, pos_red, cfg, rows=prow, bf16_storage=storage)
+            full_rows, ref_rows = [], []
+            for p, yp in zip(prow, y):
+                if p < T * Hh * ((W + 1) // 2):
+                    i0 = (p // ((W + 1) // 2)) * W + 2 * (p % ((W + 1) // 2))
+                    for i in (i0, i0 + 1):
+                        full_rows.append(i)
+                        v = x_in[i] + (yp - x_red[p])
+                        ref_rows.append(O.bf16_round(v) if storage else v)
+                else:
+                    i = p + T * Hh * (W - (W + 1) // 2)
                     full_rows.append(i)
-                    ref_rows.append(x_in[i] + (yp - x_red[p]))
-            else:
-                i = p + T * Hh * (W - (W + 1) // 2)
-                full_rows.append(i)
-                ref_rows.append(yp)
-        _check_rows(got[full_rows], np.stack(ref_rows), x_in[full_rows])
+                    ref_rows.append(yp)
+            refs.append(np.stack(ref_rows))
+        assert_block(got[full_rows], x_in[full_rows], refs[0], refs[1])
