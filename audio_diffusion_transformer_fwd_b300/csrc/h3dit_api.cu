@@ -726,3 +726,60 @@ h3dit_status h3dit_reduced_positions(const float* pos, int n_tokens, const h3dit
 }
 
 }  // extern "C"
+
+// ====================================================================== allocation-free block
+// Some callers cannot hand the library a workspace: a host program whose
+// device memory is owned by one allocator it does not expose, or a serving
+// loop that must never call cudaMalloc because that call can synchronise the
+// whole device and stall the other streams.  h3dit_block_forward_noalloc
+// serves them with a fixed scratch area that lives in the library's own
+// device image, so neither the caller nor the library allocates anything.
+namespace {
+
+// 64 MiB of block workspace (the tiny-block class and other small shapes fit;
+// a full-width block at thousands of tokens does not and is refused).  Every
+// GPU that loads the library holds this array until the process exits.
+constexpr size_t kStaticScratchBytes = size_t(64) << 20;
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+std::mutex g_static_mu;
+void* g_static_addr[64] = {nullptr};
+
+// Device address of g_static_scratch on the current device, looked up once
+// per device.  On the host the array's name only stands in for the symbol;
+// passing it to a kernel would be wrong, so the real address comes from the
+// runtime.
+h3dit_status static_scratch_address(void** out) {
+  int dev = -1;
+  H3_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(H3DIT_E_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (!g_static_addr[dev]) {
+    void* p = nullptr;
+    H3_CUDA(cudaGetSymbolAddress(&p, g_static_scratch));
+    if (!p || !aligned(p, 256)) return fail(H3DIT_E_CUDA, "static scratch address is not usable");
+    g_static_addr[dev] = p;
+  }
+  *out = g_static_addr[dev];
+  return H3DIT_OK;
+}
+
+}  // namespace
+
+extern "C" h3dit_status h3dit_block_forward_noalloc(const h3dit_config* cfg, const h3dit_block_weights* w,
+                                                    const float* mod, void* x, const float* pos, int n_tokens,
+                                                    cudaStream_t stream) {
+  H3_TRY(check_cfg(cfg));
+  if (n_tokens < 1) return fail(H3DIT_E_INVAL, "n_tokens %d", n_tokens);
+  const size_t need = plan_arena(cfg, n_tokens, nullptr).total;
+  if (need > kStaticScratchBytes)
+    return fail(H3DIT_E_NOMEM,
+                "block at %d tokens needs %zu bytes of scratch; the built-in scratch holds %zu bytes "
+                "(use h3dit_block_forward with a caller workspace)",
+                n_tokens, need, kStaticScratchBytes);
+  void* ws = nullptr;
+  H3_TRY(static_scratch_address(&ws));
+  // Nothing in the scratch has to start at zero: every byte the block reads
+  // from it is written earlier in the same call.
+  return h3dit_block_forward(cfg, w, mod, x, pos, n_tokens, ws, kStaticScratchBytes, stream);
+}

@@ -26,7 +26,7 @@ KC_ROWS, KC_QKV, KC_ATTN, KC_OPROJ, KC_FC1, KC_FC2, KC_REDUCE, KC_QUANT = range(
 _EXPORTS = [
     "h3dit_last_error", "h3dit_version", "h3dit_check_device_error",
     "h3dit_timing_enable", "h3dit_timing_reset", "h3dit_timing_read",
-    "h3dit_workspace_size", "h3dit_block_forward", "h3dit_step_forward",
+    "h3dit_workspace_size", "h3dit_block_forward", "h3dit_block_forward_noalloc", "h3dit_step_forward",
     "h3dit_quantize_act", "h3dit_quantize_weight",
     "h3dit_reduced_tokens", "h3dit_token_reduce", "h3dit_token_restore", "h3dit_reduced_positions",
     "h3dit_adaln", "h3dit_gate_residual_adaln", "h3dit_rope_table", "h3dit_qkv_project",
@@ -83,6 +83,7 @@ def lib():
             "h3dit_timing_read": (i, [i, P(ctypes.c_double), P(ctypes.c_longlong)]),
             "h3dit_workspace_size": (i, [P(Config), i, P(Reduction), P(sz)]),
             "h3dit_block_forward": (i, [P(Config), P(BlockWeights), vp, vp, vp, i, vp, sz, vp]),
+            "h3dit_block_forward_noalloc": (i, [P(Config), P(BlockWeights), vp, vp, vp, i, vp]),
             "h3dit_step_forward": (i, [P(Config), P(BlockWeights), i, vp, vp, vp, i, P(Reduction), vp, sz, vp]),
             "h3dit_quantize_act": (i, [vp, i, i, i, vp, vp, vp]),
             "h3dit_quantize_weight": (i, [vp, i, i, vp, vp, vp]),
@@ -207,6 +208,13 @@ def h3dit_block_forward(shape: BlockShape, w: BlockWeights, mod, x, pos, n_token
                         stream=None):
     _check(lib().h3dit_block_forward(ctypes.byref(shape.c()), ctypes.byref(w), _ptr(mod), _ptr(x), _ptr(pos),
                                      n_tokens, _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def h3dit_block_forward_noalloc(shape: BlockShape, w: BlockWeights, mod, x, pos, n_tokens: int, stream=None):
+    """h3dit_block_forward with the library's built-in 64 MiB scratch instead of
+    a caller workspace (for callers that cannot allocate device memory)."""
+    _check(lib().h3dit_block_forward_noalloc(ctypes.byref(shape.c()), ctypes.byref(w), _ptr(mod), _ptr(x),
+                                             _ptr(pos), n_tokens, _stream(stream)))
 
 
 def h3dit_step_forward(shape: BlockShape, ws_list: Sequence[BlockWeights], mods, x, pos, n_tokens: int,

@@ -183,6 +183,27 @@ h3dit_status h3dit_step_forward(const h3dit_config* cfg, const h3dit_block_weigh
                                 int n_tokens, const h3dit_reduction* tr, void* ws,
                                 size_t ws_bytes, cudaStream_t stream);
 
+/* The block of h3dit_block_forward for callers that cannot allocate device
+ * memory or hand over a workspace (for instance a host program whose single
+ * allocator owns all device memory, or a serving loop that must not call
+ * cudaMalloc because it can synchronise the device).  The pages have no
+ * counterpart; this is an interface convenience of this library.
+ * The scratch is a fixed 64 MiB array inside the library's device image;
+ * the caller still passes x (in/out), weights, mod and pos as above.
+ *  - The first call on each device looks up that array's device address
+ *    (and so loads the library's device code there); make that first call
+ *    before any stream capture.
+ *  - Every call on a device uses the same array, which keeps whatever the
+ *    last call left in it (nothing has to start at zero).  Calls that can
+ *    overlap on the GPU (other streams, other host threads) race on it:
+ *    serialise them.
+ *  - Shapes whose workspace (h3dit_workspace_size) exceeds 64 MiB are
+ *    refused with H3DIT_E_NOMEM before anything is enqueued.
+ * Other errors as h3dit_block_forward. */
+h3dit_status h3dit_block_forward_noalloc(const h3dit_config* cfg, const h3dit_block_weights* w,
+                                         const float* mod, void* x, const float* pos, int n_tokens,
+                                         cudaStream_t stream);
+
 /* ---------------------------------------------------------------- quantisation */
 
 /* Dynamic symmetric int8 quantisation ([linlog] "int8 量化": activations
