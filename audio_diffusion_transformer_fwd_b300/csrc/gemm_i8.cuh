@@ -1,0 +1,284 @@
+// Dynamic-int8 projections with exact integer accumulation on the BF16
+// tensor cores ([linlog] "int8 量化：从 36 秒到 19 秒": per-token activation
+// scales, per-output-channel weight scales, one activation scale per 1024
+// FC2 input channels, scaled partial sums kept per group).
+//
+// sm_103a has no integer tcgen05.mma kind, so the int8 codes are fed to
+// kind::f16 as BF16 values.  Every code is an integer in [-127, 127], exact
+// in BF16, and every product is an integer of magnitude <= 16129.  A chunk
+// of at most 1024 k-columns therefore has partial sums of magnitude
+// <= 16129 * 1024 < 2^24: every partial sum is an integer that fp32 holds
+// exactly, so the fp32 TMEM accumulator of one chunk is the exact integer
+// sum whatever order the tensor core adds in.  Each chunk is drained from
+// TMEM as soon as it is complete and combined in registers:
+//   kI8Int:   acc = sum of the chunks in int32 (exact); the output is
+//             acc * s_a[row] * s_b[col], or acc itself (kEpiAcc).
+//   kI8Group: chunk g (one activation-scale group) adds s_a[row][g] * acc_g
+//             to an fp32 sum in ascending g; the output is sum * s_b[col].
+//
+// Same pipeline as gemm_bf16_tc_kernel (128 x 256 tiles, 64-wide k-blocks in
+// a 4-deep TMA ring, one thread issuing M128 N256 K16 MMAs), except that the
+// two TMEM accumulators alternate per chunk rather than per tile, and eight
+// epilogue warps hold the tile's running sums in registers: warp w reads
+// TMEM lane quarter w % 4 and column half (w - 2) / 4, 128 columns each.
+#pragma once
+#include "gemm.cuh"
+
+namespace h3 {
+
+enum { kEpiAcc = 3 };            // raw int32 accumulator output (kI8Int only)
+enum { kI8Int = 0, kI8Group = 1 };
+
+constexpr int kI8Threads = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+constexpr int kI8MaxChunkKb = 16;  // 16 k-blocks of 64 = 1024 k-columns
+
+struct I8Args {
+  const float* sa;    // kI8Int: [M] per-row scales; kI8Group: [M][groups]
+  int groups;         // kI8Group: scales per row (= K / (chunk_kb * 64))
+  const float* sb;    // [N] per-output-channel scales
+  int chunk_kb;       // k-blocks per chunk, 1..16
+  int32_t* acc;       // kEpiAcc: [M][N] int32 output
+};
+
+// The epilogues of gemm_epilogue_chunk on 16 columns (a 16-column group
+// never straddles a head: head_dim is 64 or 128).
+template <int EPI>
+__device__ __forceinline__ void i8_epilogue16(const GemmArgs& a, const float (&v)[16], int grow, int gcol) {
+  if constexpr (EPI == kEpiStore || EPI == kEpiGelu) {
+    uint32_t p[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float x0 = v[2 * i], x1 = v[2 * i + 1];
+      if constexpr (EPI == kEpiGelu) {
+        x0 = gelu_tanh_f(x0);
+        x1 = gelu_tanh_f(x1);
+      }
+      p[i] = pack_bf16x2(x0, x1);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(a.c + static_cast<size_t>(grow) * a.ldc + gcol);
+    dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
+    dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+  } else {
+    const int region = gcol / a.d;   // 0 = Q, 1 = K, 2 = V
+    const int cin = gcol - region * a.d;
+    const int head = cin / a.head_dim;
+    const int dh0 = cin - head * a.head_dim;
+    if (region < 2) {
+      const float4* cs = reinterpret_cast<const float4*>(
+          a.rope + static_cast<size_t>(grow) * (a.head_dim / 2) + dh0 / 2);
+      uint32_t p[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 t = __ldg(cs + i);   // (cos, sin) of two consecutive pairs
+        const float a0 = v[4 * i], b0 = v[4 * i + 1], a1 = v[4 * i + 2], b1 = v[4 * i + 3];
+        p[2 * i] = pack_bf16x2(a0 * t.x - b0 * t.y, a0 * t.y + b0 * t.x);
+        p[2 * i + 1] = pack_bf16x2(a1 * t.z - b1 * t.w, a1 * t.w + b1 * t.z);
+      }
+      __nv_bfloat16* base = region == 0 ? a.q : a.k;
+      uint4* dst = reinterpret_cast<uint4*>(base + (static_cast<size_t>(head) * a.M + grow) * a.head_dim + dh0);
+      dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
+      dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+    } else {
+      __nv_bfloat16* dst = a.vt + (static_cast<size_t>(head) * a.head_dim + dh0) * a.vt_ld + grow;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) dst[static_cast<size_t>(i) * a.vt_ld] = __float2bfloat16_rn(v[i]);
+    }
+  }
+}
+
+template <int EPI, int MODE>
+__global__ void __launch_bounds__(kI8Threads, 1)
+    gemm_i8x_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                       const __grid_constant__ CUtensorMap tmB, const GemmArgs args,
+                       const I8Args qa) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kGemmStages * kGemmABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kGemmStages * kGemmStageBytes);
+  // bars: full[S], empty[S], tfull[2], tempty[2], drain
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kGemmStages + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = smem_u32(bars + kGemmStages);
+  const uint32_t tfull0 = smem_u32(bars + 2 * kGemmStages);
+  const uint32_t tempty0 = smem_u32(bars + 2 * kGemmStages + 2);
+  const uint32_t drain = smem_u32(bars + 2 * kGemmStages + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kGemmStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(tfull0 + 8 * i, 1);
+      mbar_init(tempty0 + 8 * i, 256);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), kGemmTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int kblocks = args.K / kGemmBK;
+  const int nchunks = (kblocks + qa.chunk_kb - 1) / qa.chunk_kb;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
+        int mb, nb;
+        gemm_tile_coords(t, args, mb, nb);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
+          const uint32_t fb = full0 + 8 * stage;
+          mbar_arrive_expect_tx(fb, kGemmStageBytes);
+          tma_load_2d(smem_u32(sA + stage * kGemmABytes), &tmA, fb, kb * kGemmBK, mb * kGemmBM);
+          tma_load_2d(smem_u32(sB + stage * kGemmBBytes), &tmB, fb, kb * kGemmBK, nb * kGemmBN);
+          if (++stage == kGemmStages) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < kGemmStages; ++s) mbar_wait_drain(full0 + 8 * s, phase);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer: one accumulator per chunk, alternating
+      constexpr uint32_t idesc = idesc_bf16_f32(kGemmBM, kGemmBN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int cc = 0;   // chunks issued so far by this CTA
+      bool ok = true;
+      for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
+        for (int ch = 0; ch < nchunks && ok; ++ch, ++cc) {
+          const int acc = cc & 1;
+          if (!mbar_wait(tempty0 + 8 * acc, ((cc >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + acc * kGemmBN;
+          const int kb0 = ch * qa.chunk_kb;
+          const int kb1 = min(kblocks, kb0 + qa.chunk_kb);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(sA + stage * kGemmABytes);
+            const uint32_t b0 = smem_u32(sB + stage * kGemmBBytes);
+#pragma unroll
+            for (int k = 0; k < kGemmBK / 16; ++k) {
+              tc_mma_bf16(d_tmem, sdesc_k128(a0 + 32 * k), sdesc_k128(b0 + 32 * k), idesc,
+                          (kb != kb0 || k != 0) ? 1u : 0u);
+            }
+            tc_commit(empty0 + 8 * stage);
+            if (++stage == kGemmStages) { stage = 0; phase ^= 1; }
+          }
+          if (!ok) break;
+          tc_commit(tfull0 + 8 * acc);
+        }
+      }
+      tc_commit(drain);
+      mbar_wait_drain(drain, 0);
+    }
+  } else {
+    // ---------------- epilogue warps 2..9
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int row = quarter * 32 + lane;
+    int cc = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
+      int mb, nb;
+      gemm_tile_coords(t, args, mb, nb);
+      const int grow = mb * kGemmBM + row;
+      const bool live = grow < args.M;
+      const int col0 = nb * kGemmBN + half * 128;
+      int iacc[128];
+      float facc[128];
+      for (int ch = 0; ch < nchunks; ++ch, ++cc) {
+        const int acc = cc & 1;
+        __syncwarp();
+        if (!mbar_wait(tfull0 + 8 * acc, (cc >> 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t tbase =
+            tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kGemmBN + half * 128;
+        float sg = 0.f;
+        if constexpr (MODE == kI8Group) {
+          if (live) sg = __ldg(qa.sa + static_cast<size_t>(grow) * qa.groups + ch);
+        }
+        // 16 columns per TMEM load keeps the 128 running sums plus the
+        // loaded values within the 168 registers a thread of this 10-warp
+        // CTA can have (three warps share one SM sub-partition's registers)
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          float v[16];
+          tmem_ld16(tbase + c8 * 16, v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            if constexpr (MODE == kI8Int) {
+              const int x = __float2int_rn(v[i]);   // an exact integer below 2^24
+              iacc[c8 * 16 + i] = ch == 0 ? x : iacc[c8 * 16 + i] + x;
+            } else {
+              facc[c8 * 16 + i] = ch == 0 ? v[i] * sg : fmaf(v[i], sg, facc[c8 * 16 + i]);
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(tempty0 + 8 * acc);
+      }
+      if (!ok) break;
+      if (!live) continue;
+      if constexpr (EPI == kEpiAcc) {
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          int4* dst = reinterpret_cast<int4*>(qa.acc + static_cast<size_t>(grow) * args.N + col0 + c4 * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_int4(iacc[c4 * 32 + 4 * i], iacc[c4 * 32 + 4 * i + 1], iacc[c4 * 32 + 4 * i + 2],
+                               iacc[c4 * 32 + 4 * i + 3]);
+        }
+      } else {
+        float sa = 1.f;
+        if constexpr (MODE == kI8Int) sa = __ldg(qa.sa + grow);
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          float v[16];
+          const float4* sb4 = reinterpret_cast<const float4*>(qa.sb + col0 + c8 * 16);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float4 s = __ldg(sb4 + i);
+            const float sbv[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j = c8 * 16 + 4 * i + e;
+              if constexpr (MODE == kI8Int) v[4 * i + e] = (static_cast<float>(iacc[j]) * sa) * sbv[e];
+              else v[4 * i + e] = facc[j] * sbv[e];
+            }
+          }
+          i8_epilogue16<EPI>(args, v, grow, col0 + c8 * 16);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, kGemmTmemCols);
+}
+
+}  // namespace h3

@@ -16,6 +16,7 @@
 #include "../../include/h3dit.h"
 #include "attention.cuh"
 #include "gemm.cuh"
+#include "gemm_i8.cuh"
 #include "ptx.cuh"
 #include "rows.cuh"
 
@@ -154,6 +155,9 @@ h3dit_status check_cfg(const h3dit_config* c) {
   if (!(c->rope_theta > 0.f)) return fail(H3DIT_E_INVAL, "rope_theta must be > 0");
   if (c->precision != H3DIT_BF16 && c->precision != H3DIT_INT8)
     return fail(H3DIT_E_INVAL, "precision %d", c->precision);
+  if (c->precision == H3DIT_INT8 && c->ffn > 1024 && c->ffn % 1024 != 0)
+    return fail(H3DIT_E_UNSUPPORTED, "int8 ffn %d (FC2 scale groups of 1024 need ffn <= 1024 or a multiple of 1024)",
+                c->ffn);
   return H3DIT_OK;
 }
 
@@ -195,12 +199,13 @@ h3dit_status set_smem(K kernel, size_t bytes) {
   return H3DIT_OK;
 }
 
-h3dit_status launch_gemm(int epi, const void* A, const void* B, int M, int N, int K, h3::GemmArgs args,
-                         int cls, cudaStream_t s) {
+// Tensor maps of the GEMM operands A [M][K] and B [N][K] (BF16, K-major) and
+// the tile counts; shared by the BF16 and the int8-code kernels.
+h3dit_status gemm_setup(const void* A, const void* B, int M, int N, int K, CUtensorMap& ta, CUtensorMap& tb,
+                        h3::GemmArgs& args) {
   if (M < 1 || N % h3::kGemmBN != 0 || K % h3::kGemmBK != 0 || N <= 0 || K <= 0)
     return fail(H3DIT_E_UNSUPPORTED, "gemm shape %dx%dx%d (n %% 256, k %% 64)", M, N, K);
   if (!aligned(A, 16) || !aligned(B, 16)) return fail(H3DIT_E_INVAL, "gemm operands must be 16-byte aligned");
-  CUtensorMap ta, tb;
   {
     const uint64_t dims[2] = {(uint64_t)K, (uint64_t)M};
     const uint64_t str[1] = {(uint64_t)K * 2};
@@ -219,6 +224,13 @@ h3dit_status launch_gemm(int epi, const void* A, const void* B, int M, int N, in
   args.tiles_m = (M + h3::kGemmBM - 1) / h3::kGemmBM;
   args.tiles_n = N / h3::kGemmBN;
   args.num_tiles = args.tiles_m * args.tiles_n;
+  return H3DIT_OK;
+}
+
+h3dit_status launch_gemm(int epi, const void* A, const void* B, int M, int N, int K, h3::GemmArgs args,
+                         int cls, cudaStream_t s) {
+  CUtensorMap ta, tb;
+  H3_TRY(gemm_setup(A, B, M, N, K, ta, tb, args));
   const int grid = std::min(args.num_tiles, sm_count());
   TimedLaunch tl(cls, s);
   switch (epi) {
@@ -245,6 +257,63 @@ h3dit_status launch_gemm(int epi, const void* A, const void* B, int M, int N, in
   }
   H3_CUDA(cudaGetLastError());
   return H3DIT_OK;
+}
+
+template <int EPI, int MODE>
+h3dit_status launch_i8_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const h3::GemmArgs& args,
+                              const h3::I8Args& qa, int grid, cudaStream_t s) {
+  static bool once = false;
+  if (!once) {
+    H3_TRY(set_smem(h3::gemm_i8x_tc_kernel<EPI, MODE>, h3::kGemmSmemBytes));
+    once = true;
+  }
+  h3::gemm_i8x_tc_kernel<EPI, MODE><<<grid, h3::kI8Threads, h3::kGemmSmemBytes, s>>>(ta, tb, args, qa);
+  H3_CUDA(cudaGetLastError());
+  return H3DIT_OK;
+}
+
+// Projection on int8 codes held as BF16 values (see gemm_i8.cuh).  group ==
+// K: per-row activation scales sa [M], int32 accumulation over chunks of
+// 1024; group < K: sa [M][K / group], one chunk per group (group % 64 == 0,
+// group <= 1024).  epi kEpiAcc writes the raw int32 accumulators.
+h3dit_status launch_gemm_i8(int epi, const void* A, const float* sa, int group, const void* B, const float* sb,
+                            int M, int N, int K, h3::GemmArgs args, int32_t* acc, int cls, cudaStream_t s) {
+  CUtensorMap ta, tb;
+  H3_TRY(gemm_setup(A, B, M, N, K, ta, tb, args));
+  if (K > (1 << 17)) return fail(H3DIT_E_UNSUPPORTED, "int8 k %d (the int32 accumulator bound needs k <= 131072)", K);
+  h3::I8Args qa{};
+  qa.sa = sa;
+  qa.sb = sb;
+  qa.acc = acc;
+  const bool grouped = group != K;
+  if (grouped) {
+    if (group < 64 || group % 64 != 0 || group > 1024 || K % group != 0)
+      return fail(H3DIT_E_UNSUPPORTED, "int8 group %d (a multiple of 64, <= 1024, dividing k %d)", group, K);
+    if (epi == h3::kEpiAcc) return fail(H3DIT_E_INVAL, "raw accumulators are per-row-scale only");
+    qa.chunk_kb = group / h3::kGemmBK;
+    qa.groups = K / group;
+  } else {
+    qa.chunk_kb = h3::kI8MaxChunkKb;
+    qa.groups = 1;
+  }
+  if (epi != h3::kEpiAcc && (!sa || !sb || !aligned(sb, 16)))
+    return fail(H3DIT_E_INVAL, "int8 scales missing or sb not 16-byte aligned");
+  const int grid = std::min(args.num_tiles, sm_count());
+  TimedLaunch tl(cls, s);
+  if (grouped) {
+    switch (epi) {
+      case h3::kEpiStore: return launch_i8_kernel<h3::kEpiStore, h3::kI8Group>(ta, tb, args, qa, grid, s);
+      case h3::kEpiGelu: return launch_i8_kernel<h3::kEpiGelu, h3::kI8Group>(ta, tb, args, qa, grid, s);
+      default: return fail(H3DIT_E_INVAL, "grouped int8 epilogue %d", epi);
+    }
+  }
+  switch (epi) {
+    case h3::kEpiStore: return launch_i8_kernel<h3::kEpiStore, h3::kI8Int>(ta, tb, args, qa, grid, s);
+    case h3::kEpiGelu: return launch_i8_kernel<h3::kEpiGelu, h3::kI8Int>(ta, tb, args, qa, grid, s);
+    case h3::kEpiQKV: return launch_i8_kernel<h3::kEpiQKV, h3::kI8Int>(ta, tb, args, qa, grid, s);
+    case h3::kEpiAcc: return launch_i8_kernel<h3::kEpiAcc, h3::kI8Int>(ta, tb, args, qa, grid, s);
+    default: return fail(H3DIT_E_INVAL, "int8 epilogue %d", epi);
+  }
 }
 
 h3dit_status launch_attention(const h3dit_config* c, const void* q, const void* k, const void* vt, int vt_ld,
@@ -296,22 +365,47 @@ bool fusion_disabled() {
   return v == 1;
 }
 
+// Gated residual (branch != NULL) and/or AdaLN (shift != NULL).  hs != NULL
+// selects the int8 form of the AdaLN output: h receives the row's int8 codes
+// as BF16 values and hs[row] the scale.
 h3dit_status launch_rows(void* x, const void* branch, const float* gate, const float* shift, const float* scale,
-                         void* h, int n, int d, float eps, cudaStream_t s) {
+                         void* h, float* hs, int n, int d, float eps, cudaStream_t s) {
   TimedLaunch tl(kRows, s);
   bf16* xb = static_cast<bf16*>(x);
   const bf16* bb = static_cast<const bf16*>(branch);
   bf16* hb = static_cast<bf16*>(h);
   const bool gate_on = branch != nullptr;
   const bool norm_on = shift != nullptr;
+  const bool quant = hs != nullptr;
   if (gate_on && norm_on && !fusion_disabled()) {
-    h3::gate_adaln_kernel<true, true><<<n, h3::kRowThreads, 0, s>>>(xb, bb, gate, shift, scale, hb, d, eps);
+    if (quant)
+      h3::gate_adaln_kernel<true, true, true><<<n, h3::kRowThreads, 0, s>>>(xb, bb, gate, shift, scale, hb, hs, d, eps);
+    else
+      h3::gate_adaln_kernel<true, true><<<n, h3::kRowThreads, 0, s>>>(xb, bb, gate, shift, scale, hb, nullptr, d, eps);
   } else {
     if (gate_on)
-      h3::gate_adaln_kernel<true, false><<<n, h3::kRowThreads, 0, s>>>(xb, bb, gate, nullptr, nullptr, nullptr, d, eps);
-    if (norm_on)
-      h3::gate_adaln_kernel<false, true><<<n, h3::kRowThreads, 0, s>>>(xb, nullptr, nullptr, shift, scale, hb, d, eps);
+      h3::gate_adaln_kernel<true, false><<<n, h3::kRowThreads, 0, s>>>(xb, bb, gate, nullptr, nullptr, nullptr,
+                                                                       nullptr, d, eps);
+    if (norm_on) {
+      if (quant)
+        h3::gate_adaln_kernel<false, true, true><<<n, h3::kRowThreads, 0, s>>>(xb, nullptr, nullptr, shift, scale, hb,
+                                                                               hs, d, eps);
+      else
+        h3::gate_adaln_kernel<false, true><<<n, h3::kRowThreads, 0, s>>>(xb, nullptr, nullptr, shift, scale, hb,
+                                                                         nullptr, d, eps);
+    }
   }
+  H3_CUDA(cudaGetLastError());
+  return H3DIT_OK;
+}
+
+h3dit_status launch_quantize_codes(const void* x, int rows, int cols, int group, void* q, float* scales,
+                                   cudaStream_t s) {
+  const long long blocks = 1LL * rows * (cols / group);
+  if (blocks > 0x7fffffffLL) return fail(H3DIT_E_UNSUPPORTED, "too many groups");
+  TimedLaunch tl(kQuant, s);
+  h3::quantize_codes_kernel<<<(unsigned)blocks, h3::kRowThreads, 0, s>>>(static_cast<const bf16*>(x), cols, group,
+                                                                         static_cast<bf16*>(q), scales);
   H3_CUDA(cudaGetLastError());
   return H3DIT_OK;
 }
@@ -332,14 +426,25 @@ h3dit_status launch_rope_table(const h3dit_config* c, const float* pos, int n, f
 struct Arena {
   size_t a1 = 0, a2 = 0, a3 = 0, rope = 0;     // offsets
   size_t xred = 0, rope_red = 0, pos_red = 0;  // reduction extras
+  size_t sc_row = 0, sc_grp = 0;               // int8 activation scales
   size_t total = 0;
   int vt_ld = 0;
 };
 
+// Activation-scale group of the FC2 input on the int8 path ([linlog]
+// "int8 量化": one scale per 1024 FC2 input channels; a block with F <= 1024
+// has one group).
+int fc2_group(const h3dit_config* c) { return std::min(c->ffn, 1024); }
+
 // Activation arenas aliased by lifetime ([linlog] "DiT 融合内核", activation
 // buffer aliasing):  a1 holds Q, K, V^T and then the FC1 output u; a2 holds
 // h, then the attention output o, then h2, then the next block's h; a3 holds
-// the out-projection output and then the FC2 output.
+// the out-projection output and then the FC2 output.  On the int8 path a2
+// holds int8 codes (as BF16 values) instead of h, o and h2 -- the attention
+// output goes to a3 and is quantised into a2 -- FC1's output u is quantised
+// in place in a1, and two small scale buffers are added: sc_row [N] (the
+// per-token scale of whichever projection input is live) and sc_grp
+// [N][F / 1024] (the FC2 input's group scales).
 Arena plan_arena(const h3dit_config* c, int n, const h3dit_reduction* tr) {
   Arena a;
   const size_t d = c->d, F = c->ffn;
@@ -353,6 +458,10 @@ Arena plan_arena(const h3dit_config* c, int n, const h3dit_reduction* tr) {
   a.a2 = off; off += nd;
   a.a3 = off; off += nd;
   a.rope = off; off += round_up((size_t)n * (c->head_dim / 2) * 8, 256);
+  if (c->precision == H3DIT_INT8) {
+    a.sc_row = off; off += round_up((size_t)n * 4, 256);
+    a.sc_grp = off; off += round_up((size_t)n * (F / fc2_group(c)) * 4, 256);
+  }
   if (tr) {
     const h3::PairGrid g = pair_grid(&tr->grid, n);
     a.xred = off; off += round_up((size_t)g.n_red * d * 2, 256);
@@ -367,6 +476,50 @@ struct BlockBufs {
   uint8_t* base;
   Arena ar;
 };
+
+// The dynamic-int8 block body ([linlog] "int8 量化"): QKV, out-projection
+// and FC1 take per-token int8 codes, FC2 per-token codes with one scale per
+// 1024 input channels; weights are per-output-channel int8 codes.  Attention
+// stays BF16.  Entry: a2 holds the AdaLN-1 codes and sc_row their scales.
+h3dit_status run_block_body_i8(const h3dit_config* c, const h3dit_block_weights* w, const float* mod, bf16* x,
+                               int n, const float* rope, const BlockBufs& B, int vt_ld,
+                               const float* next_shift, const float* next_scale, cudaStream_t s) {
+  const int d = c->d, F = c->ffn, dh = c->head_dim;
+  const int g2 = fc2_group(c);
+  uint8_t* a1 = B.base + B.ar.a1;
+  bf16* a2 = reinterpret_cast<bf16*>(B.base + B.ar.a2);
+  bf16* a3 = reinterpret_cast<bf16*>(B.base + B.ar.a3);
+  float* sc_row = reinterpret_cast<float*>(B.base + B.ar.sc_row);
+  float* sc_grp = reinterpret_cast<float*>(B.base + B.ar.sc_grp);
+  bf16* q = reinterpret_cast<bf16*>(a1);
+  bf16* k = reinterpret_cast<bf16*>(a1 + round_up((size_t)n * d * 2, 256));
+  bf16* vt = reinterpret_cast<bf16*>(a1 + 2 * round_up((size_t)n * d * 2, 256));
+  bf16* u = reinterpret_cast<bf16*>(a1);
+  const float* gate1 = mod + 2 * d;
+  const float* shift2 = mod + 3 * d;
+  const float* scale2 = mod + 4 * d;
+  const float* gate2 = mod + 5 * d;
+
+  h3::GemmArgs g{};
+  g.q = q; g.k = k; g.vt = vt; g.vt_ld = vt_ld; g.d = d; g.head_dim = dh;
+  g.rope = reinterpret_cast<const float2*>(rope);
+  H3_TRY(launch_gemm_i8(h3::kEpiQKV, a2, sc_row, d, w->w_qkv, w->s_qkv, n, 3 * d, d, g, nullptr, kQKV, s));
+  H3_TRY(launch_attention(c, q, k, vt, vt_ld, n, a3, s));
+  H3_TRY(launch_quantize_codes(a3, n, d, d, a2, sc_row, s));
+  h3::GemmArgs go{};
+  go.c = a3; go.ldc = d;
+  H3_TRY(launch_gemm_i8(h3::kEpiStore, a2, sc_row, d, w->w_o, w->s_o, n, d, d, go, nullptr, kOProj, s));
+  H3_TRY(launch_rows(x, a3, gate1, shift2, scale2, a2, sc_row, n, d, c->eps, s));
+  h3::GemmArgs g1{};
+  g1.c = u; g1.ldc = F;
+  H3_TRY(launch_gemm_i8(h3::kEpiGelu, a2, sc_row, d, w->w1, w->s1, n, F, d, g1, nullptr, kFC1, s));
+  H3_TRY(launch_quantize_codes(u, n, F, g2, u, sc_grp, s));
+  h3::GemmArgs gm{};
+  gm.c = a3; gm.ldc = d;
+  H3_TRY(launch_gemm_i8(h3::kEpiStore, u, sc_grp, g2, w->w2, w->s2, n, d, F, gm, nullptr, kFC2, s));
+  H3_TRY(launch_rows(x, a3, gate2, next_shift, next_scale, a2, next_shift ? sc_row : nullptr, n, d, c->eps, s));
+  return H3DIT_OK;
+}
 
 // Runs one block's sub-steps from its AdaLN output (already in a2) to the
 // final gated residual.  next_shift/next_scale: the following block's AdaLN-1
@@ -386,6 +539,8 @@ h3dit_status run_block_body(const h3dit_config* c, const h3dit_block_weights* w,
   const float* shift2 = mod + 3 * d;
   const float* scale2 = mod + 4 * d;
   const float* gate2 = mod + 5 * d;
+  if (c->precision == H3DIT_INT8)
+    return run_block_body_i8(c, w, mod, x, n, rope, B, vt_ld, next_shift, next_scale, s);
 
   h3::GemmArgs g{};
   g.q = q; g.k = k; g.vt = vt; g.vt_ld = vt_ld; g.d = d; g.head_dim = dh;
@@ -395,14 +550,14 @@ h3dit_status run_block_body(const h3dit_config* c, const h3dit_block_weights* w,
   h3::GemmArgs go{};
   go.c = a3; go.ldc = d;
   H3_TRY(launch_gemm(h3::kEpiStore, a2, w->w_o, n, d, d, go, kOProj, s));
-  H3_TRY(launch_rows(x, a3, gate1, shift2, scale2, a2, n, d, c->eps, s));
+  H3_TRY(launch_rows(x, a3, gate1, shift2, scale2, a2, nullptr, n, d, c->eps, s));
   h3::GemmArgs g1{};
   g1.c = u; g1.ldc = F;
   H3_TRY(launch_gemm(h3::kEpiGelu, a2, w->w1, n, F, d, g1, kFC1, s));
   h3::GemmArgs g2{};
   g2.c = a3; g2.ldc = d;
   H3_TRY(launch_gemm(h3::kEpiStore, u, w->w2, n, d, F, g2, kFC2, s));
-  H3_TRY(launch_rows(x, a3, gate2, next_shift, next_scale, a2, n, d, c->eps, s));
+  H3_TRY(launch_rows(x, a3, gate2, next_shift, next_scale, a2, nullptr, n, d, c->eps, s));
   (void)H;
   return H3DIT_OK;
 }
@@ -495,7 +650,8 @@ h3dit_status h3dit_adaln(const h3dit_config* cfg, const void* x, const float* sh
   H3_TRY(check_cfg(cfg));
   if (!x || !shift || !scale || !h) return fail(H3DIT_E_INVAL, "NULL pointer");
   if (n_tokens < 1) return fail(H3DIT_E_INVAL, "n_tokens %d", n_tokens);
-  return launch_rows(const_cast<void*>(x), nullptr, nullptr, shift, scale, h, n_tokens, cfg->d, cfg->eps, stream);
+  return launch_rows(const_cast<void*>(x), nullptr, nullptr, shift, scale, h, nullptr, n_tokens, cfg->d, cfg->eps,
+                     stream);
 }
 
 h3dit_status h3dit_gate_residual_adaln(const h3dit_config* cfg, void* x, const void* branch, const float* gate,
@@ -506,7 +662,7 @@ h3dit_status h3dit_gate_residual_adaln(const h3dit_config* cfg, void* x, const v
   if ((shift == nullptr) != (scale == nullptr)) return fail(H3DIT_E_INVAL, "shift and scale must both be set or NULL");
   if (shift && !h) return fail(H3DIT_E_INVAL, "h is NULL");
   if (n_tokens < 1) return fail(H3DIT_E_INVAL, "n_tokens %d", n_tokens);
-  return launch_rows(x, branch, gate, shift, scale, h, n_tokens, cfg->d, cfg->eps, stream);
+  return launch_rows(x, branch, gate, shift, scale, h, nullptr, n_tokens, cfg->d, cfg->eps, stream);
 }
 
 h3dit_status h3dit_qkv_project(const h3dit_config* cfg, const void* h, const void* w_qkv, const float* table,
@@ -555,7 +711,6 @@ h3dit_status h3dit_block_forward(const h3dit_config* cfg, const h3dit_block_weig
   H3_TRY(check_weights(cfg, w));
   if (!mod || !x || !pos || !ws) return fail(H3DIT_E_INVAL, "NULL pointer");
   if (n_tokens < 1) return fail(H3DIT_E_INVAL, "n_tokens %d", n_tokens);
-  if (cfg->precision != H3DIT_BF16) return fail(H3DIT_E_UNSUPPORTED, "int8 block not built yet");
   if (!aligned(ws, 256) || !aligned(x, 16)) return fail(H3DIT_E_INVAL, "ws must be 256-byte and x 16-byte aligned");
   const Arena ar = plan_arena(cfg, n_tokens, nullptr);
   if (ws_bytes < ar.total) return fail(H3DIT_E_NOMEM, "workspace %zu < %zu bytes", ws_bytes, ar.total);
@@ -564,7 +719,9 @@ h3dit_status h3dit_block_forward(const h3dit_config* cfg, const h3dit_block_weig
   bf16* xb = static_cast<bf16*>(x);
   const int d = cfg->d;
   H3_TRY(launch_rope_table(cfg, pos, n_tokens, rope, stream));
-  H3_TRY(launch_rows(xb, nullptr, nullptr, mod + 0 * d, mod + 1 * d, B.base + ar.a2, n_tokens, d, cfg->eps, stream));
+  float* hs = cfg->precision == H3DIT_INT8 ? reinterpret_cast<float*>(B.base + ar.sc_row) : nullptr;
+  H3_TRY(launch_rows(xb, nullptr, nullptr, mod + 0 * d, mod + 1 * d, B.base + ar.a2, hs, n_tokens, d, cfg->eps,
+                     stream));
   return run_block_body(cfg, w, mod, xb, n_tokens, rope, B, ar.vt_ld, nullptr, nullptr, stream);
 }
 
@@ -577,7 +734,6 @@ h3dit_status h3dit_step_forward(const h3dit_config* cfg, const h3dit_block_weigh
   for (int b = 0; b < n_blocks; ++b) H3_TRY(check_weights(cfg, &w[b]));
   if (!mods || !x || !pos || !ws) return fail(H3DIT_E_INVAL, "NULL pointer");
   if (n_tokens < 1) return fail(H3DIT_E_INVAL, "n_tokens %d", n_tokens);
-  if (cfg->precision != H3DIT_BF16) return fail(H3DIT_E_UNSUPPORTED, "int8 step not built yet");
   if (!aligned(ws, 256) || !aligned(x, 16)) return fail(H3DIT_E_INVAL, "ws must be 256-byte and x 16-byte aligned");
   if (tr) {
     H3_TRY(check_grid(&tr->grid, n_tokens));
@@ -614,7 +770,8 @@ h3dit_status h3dit_step_forward(const h3dit_config* cfg, const h3dit_block_weigh
   int cur_n = n_tokens;
   const float* cur_rope = rope_full;
   bool reduced = false;
-  H3_TRY(launch_rows(cur, nullptr, nullptr, mods, mods + d, B.base + ar.a2, cur_n, d, cfg->eps, stream));
+  float* hs = cfg->precision == H3DIT_INT8 ? reinterpret_cast<float*>(B.base + ar.sc_row) : nullptr;
+  H3_TRY(launch_rows(cur, nullptr, nullptr, mods, mods + d, B.base + ar.a2, hs, cur_n, d, cfg->eps, stream));
   for (int b = 0; b < n_blocks; ++b) {
     const float* mod = mods + (size_t)6 * d * b;
     const bool last = b + 1 == n_blocks;
@@ -635,7 +792,7 @@ h3dit_status h3dit_step_forward(const h3dit_config* cfg, const h3dit_block_weigh
       cur_n = pg.n_red;
       cur_rope = rope_red;
       reduced = true;
-      H3_TRY(launch_rows(cur, nullptr, nullptr, nmod, nmod + d, B.base + ar.a2, cur_n, d, cfg->eps, stream));
+      H3_TRY(launch_rows(cur, nullptr, nullptr, nmod, nmod + d, B.base + ar.a2, hs, cur_n, d, cfg->eps, stream));
     } else if (restore_now) {
       {
         TimedLaunch tl(kReduce, stream);
@@ -646,7 +803,7 @@ h3dit_status h3dit_step_forward(const h3dit_config* cfg, const h3dit_block_weigh
       cur_n = n_tokens;
       cur_rope = rope_full;
       reduced = false;
-      H3_TRY(launch_rows(cur, nullptr, nullptr, nmod, nmod + d, B.base + ar.a2, cur_n, d, cfg->eps, stream));
+      H3_TRY(launch_rows(cur, nullptr, nullptr, nmod, nmod + d, B.base + ar.a2, hs, cur_n, d, cfg->eps, stream));
     }
   }
   if (reduced) {
@@ -676,6 +833,92 @@ h3dit_status h3dit_quantize_act(const void* x_bf16, int rows, int cols, int grou
 h3dit_status h3dit_quantize_weight(const void* w_bf16, int out, int in, int8_t* q, float* scales,
                                    cudaStream_t stream) {
   return h3dit_quantize_act(w_bf16, out, in, in, q, scales, stream);
+}
+
+h3dit_status h3dit_quantize_codes(const void* x_bf16, int rows, int cols, int group, void* q_bf16, float* scales,
+                                  cudaStream_t stream) {
+  if (!x_bf16 || !q_bf16 || !scales) return fail(H3DIT_E_INVAL, "NULL pointer");
+  if (rows < 1 || cols < 1 || group < 1) return fail(H3DIT_E_INVAL, "non-positive shape");
+  if (cols % group != 0) return fail(H3DIT_E_INVAL, "group %d does not divide cols %d", group, cols);
+  if (group % 8 != 0) return fail(H3DIT_E_UNSUPPORTED, "group %d (multiple of 8)", group);
+  if (!aligned(x_bf16, 16) || !aligned(q_bf16, 16)) return fail(H3DIT_E_INVAL, "x and q must be 16-byte aligned");
+  return launch_quantize_codes(x_bf16, rows, cols, group, q_bf16, scales, stream);
+}
+
+h3dit_status h3dit_widen_codes(const int8_t* q, size_t count, void* q_bf16, cudaStream_t stream) {
+  if (!q || !q_bf16) return fail(H3DIT_E_INVAL, "NULL pointer");
+  if (count == 0) return H3DIT_OK;
+  if (count % 8 != 0) return fail(H3DIT_E_UNSUPPORTED, "count %zu (multiple of 8)", count);
+  if (!aligned(q, 8) || !aligned(q_bf16, 16)) return fail(H3DIT_E_INVAL, "q must be 8-byte, q_bf16 16-byte aligned");
+  const size_t n8 = count / 8;
+  const size_t blocks = (n8 + 255) / 256;
+  if (blocks > 0x7fffffffULL) return fail(H3DIT_E_UNSUPPORTED, "count %zu too large", count);
+  TimedLaunch tl(kQuant, stream);
+  h3::widen_codes_kernel<<<(unsigned)blocks, 256, 0, stream>>>(q, n8, static_cast<bf16*>(q_bf16));
+  H3_CUDA(cudaGetLastError());
+  return H3DIT_OK;
+}
+
+h3dit_status h3dit_adaln_quant(const h3dit_config* cfg, const void* x, const float* shift, const float* scale,
+                               int n_tokens, void* hq, float* hs, cudaStream_t stream) {
+  H3_TRY(check_cfg(cfg));
+  if (!x || !shift || !scale || !hq || !hs) return fail(H3DIT_E_INVAL, "NULL pointer");
+  if (n_tokens < 1) return fail(H3DIT_E_INVAL, "n_tokens %d", n_tokens);
+  return launch_rows(const_cast<void*>(x), nullptr, nullptr, shift, scale, hq, hs, n_tokens, cfg->d, cfg->eps,
+                     stream);
+}
+
+h3dit_status h3dit_gate_residual_adaln_quant(const h3dit_config* cfg, void* x, const void* branch, const float* gate,
+                                             const float* shift, const float* scale, int n_tokens, void* hq,
+                                             float* hs, cudaStream_t stream) {
+  H3_TRY(check_cfg(cfg));
+  if (!x || !branch || !gate || !shift || !scale || !hq || !hs) return fail(H3DIT_E_INVAL, "NULL pointer");
+  if (n_tokens < 1) return fail(H3DIT_E_INVAL, "n_tokens %d", n_tokens);
+  return launch_rows(x, branch, gate, shift, scale, hq, hs, n_tokens, cfg->d, cfg->eps, stream);
+}
+
+h3dit_status h3dit_linear_i8(const void* a_codes, const float* sa, int group, const void* b_codes, const float* sb,
+                             int m, int n, int k, int act, void* c, cudaStream_t stream) {
+  if (!a_codes || !sa || !b_codes || !sb || !c) return fail(H3DIT_E_INVAL, "NULL pointer");
+  if (m < 1 || n < 1 || k < 1) return fail(H3DIT_E_INVAL, "non-positive shape");
+  if (act != 0 && act != 1) return fail(H3DIT_E_INVAL, "act %d", act);
+  if (group < 1 || group > k) return fail(H3DIT_E_INVAL, "group %d (1..k)", group);
+  if (!aligned(c, 16)) return fail(H3DIT_E_INVAL, "c must be 16-byte aligned");
+  h3::GemmArgs g{};
+  g.c = static_cast<bf16*>(c);
+  g.ldc = n;
+  return launch_gemm_i8(act ? h3::kEpiGelu : h3::kEpiStore, a_codes, sa, group, b_codes, sb, m, n, k, g, nullptr,
+                        act ? kFC1 : kOProj, stream);
+}
+
+h3dit_status h3dit_linear_i8_acc(const void* a_codes, const void* b_codes, int m, int n, int k, int32_t* acc,
+                                 cudaStream_t stream) {
+  if (!a_codes || !b_codes || !acc) return fail(H3DIT_E_INVAL, "NULL pointer");
+  if (m < 1 || n < 1 || k < 1) return fail(H3DIT_E_INVAL, "non-positive shape");
+  if (!aligned(acc, 16)) return fail(H3DIT_E_INVAL, "acc must be 16-byte aligned");
+  h3::GemmArgs g{};
+  return launch_gemm_i8(h3::kEpiAcc, a_codes, nullptr, k, b_codes, nullptr, m, n, k, g, acc, kOProj, stream);
+}
+
+h3dit_status h3dit_qkv_project_i8(const h3dit_config* cfg, const void* hq, const float* hs, const void* w_qkv,
+                                  const float* s_qkv, const float* table, int n_tokens, void* q, void* k, void* vt,
+                                  int vt_ld, cudaStream_t stream) {
+  H3_TRY(check_cfg(cfg));
+  if (!hq || !hs || !w_qkv || !s_qkv || !table || !q || !k || !vt) return fail(H3DIT_E_INVAL, "NULL pointer");
+  if (n_tokens < 1) return fail(H3DIT_E_INVAL, "n_tokens %d", n_tokens);
+  if (vt_ld < n_tokens || vt_ld % 8 != 0) return fail(H3DIT_E_INVAL, "vt_ld %d", vt_ld);
+  if (!aligned(table, 16) || !aligned(q, 16) || !aligned(k, 16) || !aligned(vt, 16))
+    return fail(H3DIT_E_INVAL, "outputs must be 16-byte aligned");
+  h3::GemmArgs g{};
+  g.q = static_cast<bf16*>(q);
+  g.k = static_cast<bf16*>(k);
+  g.vt = static_cast<bf16*>(vt);
+  g.vt_ld = vt_ld;
+  g.d = cfg->d;
+  g.head_dim = cfg->head_dim;
+  g.rope = reinterpret_cast<const float2*>(table);
+  return launch_gemm_i8(h3::kEpiQKV, hq, hs, cfg->d, w_qkv, s_qkv, n_tokens, 3 * cfg->d, cfg->d, g, nullptr, kQKV,
+                        stream);
 }
 
 int h3dit_reduced_tokens(int n_tokens, const h3dit_video_grid* g) {

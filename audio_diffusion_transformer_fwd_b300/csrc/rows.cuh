@@ -36,15 +36,26 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
                     pack_bf16x2(f[6], f[7]));
 }
 
+// int8 code of x at scale s (s = absmax / 127 of x's group): x / s correctly
+// rounded in fp32, rounded half to even, clamped to [-127, 127]; s = 0 gives 0.
+__device__ __forceinline__ int quant_code(float x, float s) {
+  if (s == 0.f) return 0;
+  return max(-127, min(127, __float2int_rn(__fdiv_rn(x, s))));
+}
+
 // x_out = bf16(x + gate * branch) (if GATE) and h = bf16(LN(x_out)(1+scale)+shift)
 // (if NORM).  LN statistics in fp32 over the rounded row: mean, then the
 // biased variance of (x - mean) from the register copy.
-template <bool GATE, bool NORM>
+// QUANT (dynamic-int8 path, [linlog] "int8 量化"): instead of h the row's
+// int8 codes of bf16(h) at s = absmax(bf16(h)) / 127 are written into h as
+// BF16 values, and s into hs[row] -- the same codes h3dit_quantize_act gives
+// for the BF16 h.
+template <bool GATE, bool NORM, bool QUANT = false>
 __global__ void __launch_bounds__(kRowThreads)
     gate_adaln_kernel(__nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ branch,
                       const float* __restrict__ gate, const float* __restrict__ shift,
-                      const float* __restrict__ scale, __nv_bfloat16* __restrict__ h, int d,
-                      float eps) {
+                      const float* __restrict__ scale, __nv_bfloat16* __restrict__ h,
+                      float* __restrict__ hs, int d, float eps) {
   __shared__ float red[4];
   const size_t row = blockIdx.x;
   const int nvec = d >> 3;
@@ -103,9 +114,92 @@ __global__ void __launch_bounds__(kRowThreads)
       float o[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] = fmaf((v[i][e] - mean) * rstd, 1.f + sc[e], sh[e]);
-      hr[idx] = pack8(o);
+      if (QUANT) {
+        unpack8(pack8(o), v[i]);   // keep bf16(h) for the codes below
+      } else {
+        hr[idx] = pack8(o);
+      }
     }
   }
+  if (!QUANT) return;
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRowMaxVec; ++i) {
+    const int idx = i * kRowThreads + threadIdx.x;
+    if (idx < nvec) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[i][e]));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  __syncthreads();   // red[] was last read by the variance reduction
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  const float sq8 = __fdiv_rn(amax, 127.0f);
+  if (threadIdx.x == 0) hs[row] = sq8;
+#pragma unroll
+  for (int i = 0; i < kRowMaxVec; ++i) {
+    const int idx = i * kRowThreads + threadIdx.x;
+    if (idx < nvec) {
+      float c[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) c[e] = static_cast<float>(quant_code(v[i][e], sq8));
+      hr[idx] = pack8(c);   // integers in [-127, 127]: exact in BF16
+    }
+  }
+}
+
+// The quantiser of quantize_kernel writing the codes as BF16 values (the
+// operand form of the int8 projections).  q may be x itself: every thread
+// reads each 16-byte chunk it overwrites, after the group's absmax is known.
+__global__ void __launch_bounds__(kRowThreads)
+    quantize_codes_kernel(const __nv_bfloat16* x, int cols, int group, __nv_bfloat16* q,
+                          float* __restrict__ scales) {
+  __shared__ float red[4];
+  const int groups = cols / group;
+  const size_t row = blockIdx.x / groups;
+  const int g = blockIdx.x - static_cast<int>(row) * groups;
+  const size_t base = row * cols + static_cast<size_t>(g) * group;
+  const uint4* src = reinterpret_cast<const uint4*>(x + base);
+  uint4* dst = reinterpret_cast<uint4*>(q + base);
+  const int nvec = group >> 3;
+  float amax = 0.f;
+  for (int idx = threadIdx.x; idx < nvec; idx += kRowThreads) {
+    float f[8];
+    unpack8(src[idx], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  const float s = __fdiv_rn(amax, 127.0f);
+  if (threadIdx.x == 0) scales[row * groups + g] = s;
+  for (int idx = threadIdx.x; idx < nvec; idx += kRowThreads) {
+    float f[8];
+    unpack8(src[idx], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = static_cast<float>(quant_code(f[e], s));
+    dst[idx] = pack8(f);
+  }
+}
+
+// int8 codes -> the same integers as BF16 values (exact), 8 per thread.
+__global__ void widen_codes_kernel(const int8_t* __restrict__ q, size_t n8,
+                                   __nv_bfloat16* __restrict__ out) {
+  const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  const uint2 w = reinterpret_cast<const uint2*>(q)[i];
+  const uint32_t ww[2] = {w.x, w.y};
+  float f[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+    f[e] = static_cast<float>(static_cast<int8_t>((ww[e >> 2] >> (8 * (e & 3))) & 0xFFu));
+  reinterpret_cast<uint4*>(out)[i] = pack8(f);
 }
 
 // Symmetric absmax int8 quantisation of groups of `group` columns; one CTA
@@ -141,11 +235,7 @@ __global__ void __launch_bounds__(kRowThreads)
     uint32_t w[2] = {0u, 0u};
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      int c = 0;
-      if (s != 0.f) {
-        c = __float2int_rn(__fdiv_rn(f[e], s));
-        c = max(-127, min(127, c));
-      }
+      const int c = quant_code(f[e], s);
       w[e >> 2] |= (static_cast<uint32_t>(c) & 0xFFu) << (8 * (e & 3));
     }
     dst[idx] = make_uint2(w[0], w[1]);

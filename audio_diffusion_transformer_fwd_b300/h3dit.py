@@ -31,6 +31,8 @@ _EXPORTS = [
     "h3dit_reduced_tokens", "h3dit_token_reduce", "h3dit_token_restore", "h3dit_reduced_positions",
     "h3dit_adaln", "h3dit_gate_residual_adaln", "h3dit_rope_table", "h3dit_qkv_project",
     "h3dit_attention", "h3dit_linear",
+    "h3dit_quantize_codes", "h3dit_widen_codes", "h3dit_linear_i8", "h3dit_linear_i8_acc",
+    "h3dit_adaln_quant", "h3dit_gate_residual_adaln_quant", "h3dit_qkv_project_i8",
 ]
 
 
@@ -97,6 +99,13 @@ def lib():
             "h3dit_qkv_project": (i, [P(Config), vp, vp, vp, i, vp, vp, vp, i, vp]),
             "h3dit_attention": (i, [P(Config), vp, vp, vp, i, i, vp, vp]),
             "h3dit_linear": (i, [vp, vp, i, i, i, i, vp, vp]),
+            "h3dit_quantize_codes": (i, [vp, i, i, i, vp, vp, vp]),
+            "h3dit_widen_codes": (i, [vp, sz, vp, vp]),
+            "h3dit_linear_i8": (i, [vp, vp, i, vp, vp, i, i, i, i, vp, vp]),
+            "h3dit_linear_i8_acc": (i, [vp, vp, i, i, i, vp, vp]),
+            "h3dit_adaln_quant": (i, [P(Config), vp, vp, vp, i, vp, vp, vp]),
+            "h3dit_gate_residual_adaln_quant": (i, [P(Config), vp, vp, vp, vp, vp, i, vp, vp, vp]),
+            "h3dit_qkv_project_i8": (i, [P(Config), vp, vp, vp, vp, vp, i, vp, vp, vp, i, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -281,3 +290,40 @@ def h3dit_attention(shape: BlockShape, q, k, vt, vt_ld: int, n_tokens: int, o, s
 
 def h3dit_linear(a, b, m: int, n: int, k: int, act: int, c, stream=None):
     _check(lib().h3dit_linear(_ptr(a), _ptr(b), m, n, k, act, _ptr(c), _stream(stream)))
+
+
+def h3dit_quantize_codes(x, rows: int, cols: int, group: int, q, scales, stream=None):
+    _check(lib().h3dit_quantize_codes(_ptr(x), rows, cols, group, _ptr(q), _ptr(scales), _stream(stream)))
+
+
+def h3dit_widen_codes(q, count: int, out, stream=None):
+    _check(lib().h3dit_widen_codes(_ptr(q), count, _ptr(out), _stream(stream)))
+
+
+def h3dit_linear_i8(a_codes, sa, group: int, b_codes, sb, m: int, n: int, k: int, act: int, c, stream=None):
+    _check(lib().h3dit_linear_i8(_ptr(a_codes), _ptr(sa), group, _ptr(b_codes), _ptr(sb), m, n, k, act, _ptr(c),
+                                 _stream(stream)))
+
+
+def h3dit_linear_i8_acc(a_codes, b_codes, m: int, n: int, k: int, acc, stream=None):
+    _check(lib().h3dit_linear_i8_acc(_ptr(a_codes), _ptr(b_codes), m, n, k, _ptr(acc), _stream(stream)))
+
+
+def h3dit_adaln_quant(shape: BlockShape, x, shift, scale, n_tokens: int, hq, hs, stream=None):
+    c = shape.c()
+    _check(lib().h3dit_adaln_quant(ctypes.byref(c), _ptr(x), _ptr(shift), _ptr(scale), n_tokens, _ptr(hq), _ptr(hs),
+                                   _stream(stream)))
+
+
+def h3dit_gate_residual_adaln_quant(shape: BlockShape, x, branch, gate, shift, scale, n_tokens: int, hq, hs,
+                                    stream=None):
+    c = shape.c()
+    _check(lib().h3dit_gate_residual_adaln_quant(ctypes.byref(c), _ptr(x), _ptr(branch), _ptr(gate), _ptr(shift),
+                                                 _ptr(scale), n_tokens, _ptr(hq), _ptr(hs), _stream(stream)))
+
+
+def h3dit_qkv_project_i8(shape: BlockShape, hq, hs, w_qkv, s_qkv, table, n_tokens: int, q, k, vt, vt_ld: int,
+                         stream=None):
+    c = shape.c()
+    _check(lib().h3dit_qkv_project_i8(ctypes.byref(c), _ptr(hq), _ptr(hs), _ptr(w_qkv), _ptr(s_qkv), _ptr(table),
+                                      n_tokens, _ptr(q), _ptr(k), _ptr(vt), vt_ld, _stream(stream)))

@@ -80,9 +80,13 @@ typedef struct {
 
 /* One block's projection weights, device pointers.
  * BF16 precision: BF16 [out][in] matrices, scale pointers unused (may be NULL).
- * INT8 precision: int8 codes [out][in] and fp32 per-output-channel scales
- *   (h3dit_quantize_weight), as in [linlog] "int8 量化" (per-output-channel
- *   weight scales).
+ * INT8 precision: per-output-channel int8 codes [out][in] in operand form --
+ *   each code stored as the BF16 value of the same integer (exact), the form
+ *   the tensor cores read, made once from int8 codes by h3dit_widen_codes --
+ *   and fp32 per-output-channel scales (h3dit_quantize_weight), as in [linlog]
+ *   "int8 量化" (per-output-channel weight scales).  sm_103a has no integer
+ *   tensor-core MMA; the int8 products are run exactly on the BF16 path (see
+ *   h3dit_linear_i8).
  *   w_qkv [3d][d]  rows 0..d-1 give Q (head h = rows h*Dh..), d..2d-1 K, 2d..3d-1 V
  *   w_o   [d][d]   attention output projection
  *   w1    [F][d]   MLP FC1
@@ -164,6 +168,12 @@ h3dit_status h3dit_workspace_size(const h3dit_config* cfg, int n_tokens,
  * x:   device BF16 [n_tokens][d], read and overwritten.
  * pos: device fp32 [n_tokens][3] (t, y, x) rotary positions.
  * ws:  device workspace of at least h3dit_workspace_size bytes, 256-byte aligned.
+ * With precision H3DIT_INT8 the four projections run on int8 codes
+ * ([linlog] "int8 量化"): h, o and h2 are quantised per token, u per token and
+ * per 1024 channels (h3dit_quantize_act's rule on their BF16 values), the
+ * weights are operand-form codes with per-output-channel scales, and the
+ * outputs are dequantised to BF16 as h3dit_linear_i8 states; attention stays
+ * BF16.  INT8 needs ffn <= 1024 or ffn % 1024 == 0.
  * Errors: E_INVAL (nulls, n_tokens < 1), E_UNSUPPORTED (shape outside the
  * limits of h3dit_config), E_NOMEM (ws_bytes too small), E_CUDA. */
 h3dit_status h3dit_block_forward(const h3dit_config* cfg, const h3dit_block_weights* w,
@@ -221,6 +231,43 @@ h3dit_status h3dit_quantize_act(const void* x_bf16, int rows, int cols, int grou
  * h3dit_quantize_act with one group per row of w [out][in]. */
 h3dit_status h3dit_quantize_weight(const void* w_bf16, int out, int in, int8_t* q,
                                    float* scales, cudaStream_t stream);
+
+/* The quantiser of h3dit_quantize_act writing each code as the BF16 value of
+ * the same integer (the operand form of the int8 projections).  q_bf16 may
+ * be x_bf16 itself (in place).  x_bf16, q_bf16: device BF16 [rows][cols],
+ * 16-byte aligned; scales: device fp32 [rows][cols / group]. */
+h3dit_status h3dit_quantize_codes(const void* x_bf16, int rows, int cols, int group,
+                                  void* q_bf16, float* scales, cudaStream_t stream);
+
+/* int8 codes -> operand form: out[i] = (bf16) q[i], exact.  q: device int8,
+ * 8-byte aligned; q_bf16: device BF16, 16-byte aligned; count % 8 == 0. */
+h3dit_status h3dit_widen_codes(const int8_t* q, size_t count, void* q_bf16,
+                               cudaStream_t stream);
+
+/* Int8 projection on operand-form codes ([linlog] "int8 量化": per-token
+ * activation scales, per-output-channel weight scales, FC2 input with one
+ * scale per 1024 channels and its scaled partial sums combined per group):
+ *   group == k:  c[t][o] = bf16(act(acc[t][o] * sa[t] * sb[o])), sa [m]
+ *   group <  k:  c[t][o] = bf16(act(sb[o] * sum_g sa[t][g] * acc_g[t][o])),
+ *                sa [m][k / group], g ascending, sums in fp32
+ * acc / acc_g are the exact integer sums of a_codes[t][j] * b_codes[o][j] over
+ * all j, or over j in group g.  The tensor cores accumulate in fp32, which is
+ * exact for integers below 2^24; every chunk of at most 1024 k-columns stays
+ * below that (127^2 * 1024 < 2^24) and is drained and added in int32.
+ * a_codes: device BF16 [m][k]; b_codes: device BF16 [n][k]; sb: device fp32
+ * [n], 16-byte aligned; c: device BF16 [m][n].  act 0 none, 1 GELU (tanh).
+ * n % 256 == 0, k % 64 == 0, k <= 131072; group < k needs group % 64 == 0,
+ * group <= 1024 and group | k.  Codes outside [-127, 127] are the caller's
+ * error (the exactness bound assumes them). */
+h3dit_status h3dit_linear_i8(const void* a_codes, const float* sa, int group,
+                             const void* b_codes, const float* sb, int m, int n, int k,
+                             int act, void* c, cudaStream_t stream);
+
+/* The exact int32 accumulators of h3dit_linear_i8 (group == k) without any
+ * scaling: acc[t][o] = sum_j a_codes[t][j] * b_codes[o][j].  acc: device int32
+ * [m][n], 16-byte aligned.  Shape limits as h3dit_linear_i8. */
+h3dit_status h3dit_linear_i8_acc(const void* a_codes, const void* b_codes, int m, int n, int k,
+                                 int32_t* acc, cudaStream_t stream);
 
 /* ---------------------------------------------------------------- token reduction */
 
@@ -292,6 +339,30 @@ h3dit_status h3dit_qkv_project(const h3dit_config* cfg, const void* h, const voi
 h3dit_status h3dit_attention(const h3dit_config* cfg, const void* q, const void* k,
                              const void* vt, int vt_ld, int n_tokens, void* o,
                              cudaStream_t stream);
+
+/* AdaLN followed by per-token dynamic int8 quantisation (the int8 path's
+ * AdaLN, [linlog] "int8 量化"): hq receives the codes of h3dit_adaln's BF16 h
+ * (the rule of h3dit_quantize_act, one group per row) as BF16 values and
+ * hs [n] the scales.  x, hq: device BF16 [n][d]; shift, scale: fp32 [d]. */
+h3dit_status h3dit_adaln_quant(const h3dit_config* cfg, const void* x, const float* shift,
+                               const float* scale, int n_tokens, void* hq, float* hs,
+                               cudaStream_t stream);
+
+/* h3dit_gate_residual_adaln with the AdaLN output quantised as in
+ * h3dit_adaln_quant (x updated in place as there). */
+h3dit_status h3dit_gate_residual_adaln_quant(const h3dit_config* cfg, void* x, const void* branch,
+                                             const float* gate, const float* shift,
+                                             const float* scale, int n_tokens, void* hq,
+                                             float* hs, cudaStream_t stream);
+
+/* h3dit_qkv_project on the int8 path: the projection is h3dit_linear_i8 of
+ * the AdaLN codes hq (BF16 [n][d]) with per-token scales hs [n] and the
+ * operand-form weight codes w_qkv [3d][d] with scales s_qkv [3d]; RoPE and
+ * the head-major outputs as h3dit_qkv_project. */
+h3dit_status h3dit_qkv_project_i8(const h3dit_config* cfg, const void* hq, const float* hs,
+                                  const void* w_qkv, const float* s_qkv, const float* table,
+                                  int n_tokens, void* q, void* k, void* vt, int vt_ld,
+                                  cudaStream_t stream);
 
 /* Projection c = act(a b^T): a BF16 [m][k], b BF16 [n][k] (a Linear weight),
  * c BF16 [m][n]; act 0 = none, 1 = GELU tanh form.  n % 256 == 0,

@@ -57,6 +57,19 @@ def test_host_only_calls(lib):
     assert "ffn" in H.lib().h3dit_last_error().decode()
 
 
+def test_int8_shape_checks_on_host():
+    w = (256, 4, 64)
+    ok = H.BlockShape(*w, 1024, precision=H.INT8, rope_sections=(16, 24, 24))
+    assert H.h3dit_workspace_size(ok, 16) > H.h3dit_workspace_size(
+        H.BlockShape(*w, 1024, rope_sections=(16, 24, 24)), 16)
+    bad = H.BlockShape(*w, 1280, precision=H.INT8, rope_sections=(16, 24, 24))
+    with pytest.raises(H.H3DitError) as e:
+        H.h3dit_workspace_size(bad, 16)
+    assert e.value.status == H.E_UNSUPPORTED
+    # the same ffn is fine in BF16
+    H.h3dit_workspace_size(H.BlockShape(*w, 1280, rope_sections=(16, 24, 24)), 16)
+
+
 def test_workspace_aliasing_saves_memory():
     """Arena aliasing keeps the block's activations to roughly
     max(3Nd + V^T padding, NF) + 2Nd BF16 values plus the RoPE table."""

@@ -1,0 +1,304 @@
+"""Parity of the dynamic-int8 path on the GPU through the C ABI against the
+oracle ([linlog] "int8 量化：从 36 秒到 19 秒").
+
+* Integer work is bit-exact: the int32 accumulators of the int8 projection
+  (random codes, codes at the +-127 extremes where every 1024-column chunk
+  comes within 2^18 of the 2^24 fp32-exactness bound, and mixes of large and
+  +-1 products whose low bits a lossy accumulator would drop), the
+  quantiser's codes and scales, the widening of int8 codes, and the codes the
+  fused AdaLN + quantise kernels emit for the BF16 h the plain AdaLN gives.
+* Dequantised projections (per-token scales; FC2's one scale per 1024
+  channels) are within relative L2 <= 2e-3 of the oracle's identical scheme
+  fed the same codes and scales: the only difference is the fp32 scaling and
+  one BF16 rounding of the output (<= 2^-9 relative per element).
+* The whole int8 block against the oracle's int8 block (same quantisation
+  scheme, BF16 storage points): the per-block acceptance bounds of the BF16
+  block.  The two sides round h, o, h2 and u independently before
+  quantising, so a code can differ by one where a value sits at a rounding
+  boundary; the block bound covers that.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from audio_diffusion_transformer_fwd_b300 import h3dit as H
+from audio_diffusion_transformer_fwd_b300 import synth
+from tests.gpu_util import dev_bf16, dev_f32, host, max_abs, oracle_cfg, rel_l2, shape_of
+from tests.test_gpu_block import assert_block
+
+pytestmark = pytest.mark.gpu
+
+TINY = synth.WORKLOADS["tiny_block"]
+
+
+def codes_dev(q: np.ndarray) -> torch.Tensor:
+    """int8 codes -> device operand form (BF16 values of the same integers)."""
+    return torch.from_numpy(np.ascontiguousarray(q, np.float32)).to("cuda").to(torch.bfloat16)
+
+
+def exact_acc(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    return O.gemm_int(a, b)
+
+
+def gpu_acc(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    m, k = a.shape
+    n = b.shape[0]
+    acc = torch.empty((m, n), device="cuda", dtype=torch.int32)
+    H.h3dit_linear_i8_acc(codes_dev(a), codes_dev(b), m, n, k, acc)
+    H.h3dit_check_device_error()
+    return acc.cpu().numpy().astype(np.int64)
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 256, 64), (129, 256, 1024), (300, 512, 1088),
+                                   (200, 256, 5120), (77, 256, 20480), (1000, 768, 2048)])
+def test_acc_bit_exact_random(m, n, k):
+    a = synth.host_int8((m, k), seed=m, stream=1)
+    b = synth.host_int8((n, k), seed=n, stream=2)
+    got = gpu_acc(a, b)
+    assert np.array_equal(got, exact_acc(a, b))
+
+
+def test_acc_bit_exact_extremes():
+    """Every 1024-column chunk of row 0 sums to 127^2 * 1024 = 16516096, of
+    row 1 to -16516096; rows 2-3 put +-1 products after 1000 products of
+    127^2 (a partial sum of 16129000, where an accumulator keeping fewer than
+    24 significant bits would drop the ones); rows 4+ are random signs of
+    +-127 against +-127 and +-1."""
+    k, n, m = 5120, 256, 160
+    a = np.full((m, k), 127, np.int8)
+    b = np.full((n, k), 127, np.int8)
+    a[1] = -127
+    for r in (2, 3):
+        for c0 in range(0, k, 1024):
+            a[r, c0 + 1000:c0 + 1024] = 1 if r == 2 else -1
+    b[1::2, :] = -127
+    for c0 in range(0, k, 1024):
+        b[2::4, c0 + 1000:c0 + 1024] = 1
+    rs = synth.host_int8((m - 4, k), seed=7, stream=3, lo=-1, hi=1)
+    a[4:] = np.where(rs >= 0, 127, -127).astype(np.int8)
+    a[4:, ::7] = np.where(rs[:, ::7] > 0, 1, -1).astype(np.int8)
+    got = gpu_acc(a, b)
+    ref = exact_acc(a, b)
+    assert abs(int(ref[0, 0])) == 5 * 16516096
+    assert np.array_equal(got, ref)
+
+
+def _dequant_case(m, n, k, group, act, seed):
+    a = synth.host_int8((m, k), seed=seed, stream=4)
+    b = synth.host_int8((n, k), seed=seed, stream=5)
+    ng = k // group
+    sa = synth.host_uniform((m, ng), seed=seed, stream=6, lo=1e-3, hi=3e-2)
+    sb = synth.host_uniform((n,), seed=seed, stream=7, lo=1e-4, hi=2e-3)
+    c = torch.empty((m, n), device="cuda", dtype=torch.bfloat16)
+    H.h3dit_linear_i8(codes_dev(a), dev_f32(sa), group, codes_dev(b), dev_f32(sb), m, n, k, act, c)
+    H.h3dit_check_device_error()
+    if group == k:
+        ref = O.linear_int8(a, sa[:, 0], b, sb)
+    else:
+        ref = O.fc2_int8(a, sa, b, sb, group)
+    if act:
+        ref = O.gelu_tanh(ref)
+    return host(c), O.bf16_round(ref)
+
+
+@pytest.mark.parametrize("m,n,k,act", [(129, 256, 1024, 0), (300, 512, 5120, 0), (77, 256, 256, 1),
+                                       (256, 768, 2048, 1)])
+def test_linear_i8_per_token(m, n, k, act):
+    got, ref = _dequant_case(m, n, k, k, act, seed=m + k)
+    assert rel_l2(got, ref) <= 2e-3
+    assert max_abs(got, ref) <= 2.0 ** -8 * float(np.max(np.abs(ref))) + 1e-6
+
+
+@pytest.mark.parametrize("m,n,k,group", [(129, 256, 4096, 1024), (300, 256, 20480, 1024),
+                                         (64, 512, 1024, 256)])
+def test_linear_i8_grouped(m, n, k, group):
+    got, ref = _dequant_case(m, n, k, group, 0, seed=m + group)
+    assert rel_l2(got, ref) <= 2e-3
+    assert max_abs(got, ref) <= 2.0 ** -8 * float(np.max(np.abs(ref))) + 1e-6
+
+
+@pytest.mark.parametrize("rows,cols,group", [(64, 1024, 1024), (37, 4096, 1024), (5, 256, 256)])
+def test_quantize_codes_bit_exact(rows, cols, group):
+    x = synth.host_activations(rows, cols, seed=rows) * np.float32(3.0)
+    x = synth.to_bf16_values(x)
+    x[1, :group] = 0.0                       # an all-zero group
+    xd = dev_bf16(x)
+    q = torch.empty_like(xd)
+    s = torch.empty((rows, cols // group), device="cuda", dtype=torch.float32)
+    H.h3dit_quantize_codes(xd, rows, cols, group, q, s)
+    qr, sr = O.quantize_rows(x, group)
+    assert np.array_equal(host(q).astype(np.int64), qr.astype(np.int64))
+    assert np.array_equal(s.cpu().numpy(), sr)
+    # in place gives the same codes
+    s2 = torch.empty_like(s)
+    H.h3dit_quantize_codes(xd, rows, cols, group, xd, s2)
+    H.h3dit_check_device_error()
+    assert np.array_equal(host(xd).astype(np.int64), qr.astype(np.int64))
+    assert np.array_equal(s2.cpu().numpy(), sr)
+
+
+def test_widen_codes_exact():
+    q = synth.host_int8((1000, 64), seed=3, stream=9)
+    qd = torch.from_numpy(q).to("cuda")
+    out = torch.empty(q.shape, device="cuda", dtype=torch.bfloat16)
+    H.h3dit_widen_codes(qd, q.size, out)
+    H.h3dit_check_device_error()
+    assert np.array_equal(host(out).astype(np.int64), q.astype(np.int64))
+
+
+@pytest.mark.parametrize("n", [256, 33])
+def test_adaln_quant_codes_match_quantised_adaln(n):
+    w = TINY
+    shape = shape_of(w, H.INT8)
+    x = synth.host_activations(n, w.d, seed=4)
+    mod = synth.host_mod(w.d, seed=4)
+    xd = dev_bf16(x)
+    h = torch.empty_like(xd)
+    H.h3dit_adaln(shape, xd, dev_f32(mod[0]), dev_f32(mod[1]), n, h)
+    hq = torch.empty_like(xd)
+    hs = torch.empty(n, device="cuda", dtype=torch.float32)
+    H.h3dit_adaln_quant(shape, xd, dev_f32(mod[0]), dev_f32(mod[1]), n, hq, hs)
+    H.h3dit_check_device_error()
+    qr, sr = O.quantize_rows(host(h))
+    assert np.array_equal(host(hq).astype(np.int64), qr.astype(np.int64))
+    assert np.array_equal(hs.cpu().numpy(), sr[:, 0])
+    # and the BF16 h itself is the oracle's AdaLN to one BF16 rounding
+    ref = O.adaln(x, mod[0], mod[1], w.eps)
+    assert max_abs(host(h), ref) <= 2.0 ** -8 * float(np.max(np.abs(ref))) + 1e-6
+
+
+def test_gate_residual_adaln_quant():
+    w = TINY
+    n = 200
+    shape = shape_of(w, H.INT8)
+    x = synth.host_activations(n, w.d, seed=5)
+    br = synth.host_activations(n, w.d, seed=6)
+    mod = synth.host_mod(w.d, seed=5, std=0.5)
+    gate, shift, scale = (dev_f32(mod[i]) for i in (2, 3, 4))
+    x_plain = dev_bf16(x)
+    h = torch.empty_like(x_plain)
+    H.h3dit_gate_residual_adaln(shape, x_plain, dev_bf16(br), gate, shift, scale, n, h)
+    x_q = dev_bf16(x)
+    hq = torch.empty_like(x_q)
+    hs = torch.empty(n, device="cuda", dtype=torch.float32)
+    H.h3dit_gate_residual_adaln_quant(shape, x_q, dev_bf16(br), gate, shift, scale, n, hq, hs)
+    H.h3dit_check_device_error()
+    assert torch.equal(x_plain, x_q)
+    qr, sr = O.quantize_rows(host(h))
+    assert np.array_equal(host(hq).astype(np.int64), qr.astype(np.int64))
+    assert np.array_equal(hs.cpu().numpy(), sr[:, 0])
+
+
+def _int8_weights(wt):
+    """Per-output-channel int8 weights of the BF16 block weights (the
+    oracle's quantiser), as host codes/scales and device operand form."""
+    hw, dev = {}, {}
+    for name, qn, sn in (("w_qkv", "q_qkv", "s_qkv"), ("w_o", "q_o", "s_o"), ("w1", "q1", "s1"), ("w2", "q2", "s2")):
+        q, s = O.quantize_weight(wt[name])
+        hw[qn], hw[sn] = q, s[:, 0]
+        dev[qn], dev[sn] = codes_dev(q), dev_f32(s[:, 0])
+    bw = H.block_weights(dev["q_qkv"], dev["q_o"], dev["q1"], dev["q2"], dev["s_qkv"], dev["s_o"], dev["s1"], dev["s2"])
+    return hw, dev, bw
+
+
+def test_qkv_project_i8():
+    w = TINY
+    n = 256
+    shape = shape_of(w, H.INT8)
+    pos = synth.positions(w.video, w.n_text, w.n_audio)
+    wt = synth.host_block_weights(w.d, w.ffn, seed=8)
+    hw, dev, _ = _int8_weights(wt)
+    h = synth.host_activations(n, w.d, seed=8)
+    hq, hs = O.quantize_rows(h)
+    table = torch.empty((n, w.head_dim // 2, 2), device="cuda", dtype=torch.float32)
+    H.h3dit_rope_table(shape, dev_f32(pos), n, table)
+    vt_ld = 256
+    q = torch.empty((w.heads, n, w.head_dim), device="cuda", dtype=torch.bfloat16)
+    k = torch.empty_like(q)
+    vt = torch.empty((w.heads, w.head_dim, vt_ld), device="cuda", dtype=torch.bfloat16)
+    H.h3dit_qkv_project_i8(shape, codes_dev(hq), dev_f32(hs[:, 0]), dev["q_qkv"], dev["s_qkv"], table, n,
+                           q, k, vt, vt_ld)
+    H.h3dit_check_device_error()
+    cfg = oracle_cfg(w)
+    qkv = O.linear_int8(hq, hs[:, 0], hw["q_qkv"], hw["s_qkv"])
+    d = w.d
+    tok = lambda t: t.reshape(n, w.heads, w.head_dim)     # [N, H, Dh]
+    rq = O.apply_rope(tok(qkv[:, :d]), pos, cfg).transpose(1, 0, 2)
+    rk = O.apply_rope(tok(qkv[:, d:2 * d]), pos, cfg).transpose(1, 0, 2)
+    rv = tok(qkv[:, 2 * d:]).transpose(1, 2, 0)
+    for got, ref in ((host(q), rq), (host(k), rk), (host(vt)[:, :, :n], rv)):
+        assert rel_l2(got, ref) <= 2e-3
+        assert max_abs(got, ref) <= 2.0 ** -8 * float(np.max(np.abs(ref))) + 1e-6
+
+
+def _run_int8_block(w, x, bw, mod, pos, n):
+    shape = shape_of(w, H.INT8)
+    xd = dev_bf16(x)
+    nbytes = H.h3dit_workspace_size(shape, n)
+    ws = torch.empty(nbytes, device="cuda", dtype=torch.uint8)
+    H.h3dit_block_forward(shape, bw, dev_f32(mod), xd, dev_f32(pos), n, ws, nbytes)
+    H.h3dit_check_device_error()
+    return host(xd)
+
+
+@pytest.mark.parametrize("n,std", [(256, 1.0), (129, 1.0), (256, 4.0)])
+def test_int8_block_tiny(n, std):
+    w = TINY
+    pos = synth.positions(w.video, w.n_text, w.n_audio)[:n]
+    x = synth.host_activations(n, w.d, seed=11)
+    wt = synth.host_block_weights(w.d, w.ffn, seed=11)
+    mod = synth.host_mod(w.d, seed=11, std=0.1 * std)
+    hw, _, bw = _int8_weights(wt)
+    got = _run_int8_block(w, x, bw, mod, pos, n)
+    cfg = oracle_cfg(w)
+    ref_bf = O.block_forward_int8(x, hw, mod, pos, cfg, bf16_storage=True)
+    ref64 = O.block_forward_int8(x, hw, mod, pos, cfg, bf16_storage=False)
+    assert_block(got, x, ref64, ref_bf)
+
+
+def test_int8_block_zero_gates_identity():
+    w = TINY
+    n = w.n_tokens
+    pos = synth.positions(w.video, w.n_text, w.n_audio)
+    x = synth.host_activations(n, w.d, seed=12)
+    wt = synth.host_block_weights(w.d, w.ffn, seed=12)
+    mod = synth.host_mod(w.d, seed=12)
+    mod[2] = 0.0
+    mod[5] = 0.0
+    _, _, bw = _int8_weights(wt)
+    got = _run_int8_block(w, x, bw, mod, pos, n)
+    assert np.array_equal(got, x)
+
+
+def test_int8_step_of_one_block_equals_block_and_chains():
+    w = TINY
+    n = w.n_tokens
+    shape = shape_of(w, H.INT8)
+    pos = synth.positions(w.video, w.n_text, w.n_audio)
+    x = synth.host_activations(n, w.d, seed=13)
+    nb = 3
+    wts = [synth.host_block_weights(w.d, w.ffn, seed=13, block=b) for b in range(nb)]
+    mods = np.stack([synth.host_mod(w.d, seed=13, block=b) for b in range(nb)])
+    packs = [_int8_weights(wt) for wt in wts]
+    # step of nb blocks vs nb block calls: bit-identical (the fused hand-over
+    # of the next AdaLN codes is the same arithmetic as the separate AdaLN)
+    xs = dev_bf16(x)
+    nbytes = H.h3dit_workspace_size(shape, n)
+    ws = torch.empty(nbytes, device="cuda", dtype=torch.uint8)
+    H.h3dit_step_forward(shape, [p[2] for p in packs], dev_f32(mods), xs, dev_f32(pos), n, None, ws, nbytes)
+    xb = dev_bf16(x)
+    for b in range(nb):
+        H.h3dit_block_forward(shape, packs[b][2], dev_f32(mods[b]), xb, dev_f32(pos), n, ws, nbytes)
+    H.h3dit_check_device_error()
+    assert torch.equal(xs, xb)
+    # and the chain follows the oracle's int8 step
+    cfg = oracle_cfg(w)
+    ref_bf = x.astype(np.float64)
+    ref64 = x.astype(np.float64)
+    for b in range(nb):
+        ref_bf = O.block_forward_int8(ref_bf, packs[b][0], mods[b], pos, cfg, bf16_storage=True)
+        ref64 = O.block_forward_int8(ref64, packs[b][0], mods[b], pos, cfg, bf16_storage=False)
+    got = host(xs)
+    assert rel_l2(got, ref_bf) <= 1e-2 * nb
+    assert rel_l2(got - x, ref_bf - x) <= 2e-2 * nb
