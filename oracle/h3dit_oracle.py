@@ -421,8 +421,17 @@ def quantize_weight(w):
 
 
 def gemm_int(aq, bq) -> np.ndarray:
-    """Exact integer product acc[t, n] = sum_k a[t, k] * b[n, k] in int64."""
-    return np.asarray(aq, np.int64) @ np.asarray(bq, np.int64).T
+    """Exact integer product acc[t, n] = sum_k a[t, k] * b[n, k], as int64.
+
+    Computed with a float64 matmul: the operands are integers of magnitude
+    <= 127, so every product and every partial sum is an integer of
+    magnitude <= 127^2 * K, far below 2^53 for any K here; float64 holds all
+    of them exactly and the result is the exact integer sum in any summation
+    order (the same value an int64 matmul gives, at BLAS speed)."""
+    a = np.asarray(aq, np.float64)
+    b = np.asarray(bq, np.float64)
+    assert a.shape[1] == b.shape[1] and 127 * 127 * a.shape[1] < 2 ** 53
+    return (a @ b.T).astype(np.int64)
 
 
 def linear_int8(xq, xs, wq, ws) -> np.ndarray:
@@ -448,13 +457,16 @@ def fc2_int8(uq, us, wq, ws, group: int = 1024) -> np.ndarray:
 
 
 def block_forward_int8(x, w: Dict[str, np.ndarray], mod, pos, cfg: BlockConfig,
-                       bf16_storage: bool = True, fc2_group: int = 1024, return_parts: bool = False):
+                       bf16_storage: bool = True, fc2_group: int = 1024, return_parts: bool = False,
+                       rows=None):
     """The block of ``block_forward`` on the dynamic-int8 path.
 
     w holds int8 codes ``q_qkv, q_o, q1, q2`` and fp32 per-output-channel
     scales ``s_qkv, s_o, s1, s2``.  QKV, out-projection and FC1 quantise their
     input per token; FC2 quantises per token and per ``fc2_group`` input
-    channels.  Attention itself stays in floating point."""
+    channels.  Attention itself stays in floating point.  ``rows`` evaluates
+    the output only for those query rows (every quantisation after QKV is per
+    token, so the rows are independent once keys and values exist)."""
     R = lambda a: _maybe_round(a, bf16_storage)
     x = np.asarray(x, dtype=np.float64)
     mod = np.asarray(mod, dtype=np.float64)
@@ -468,10 +480,11 @@ def block_forward_int8(x, w: Dict[str, np.ndarray], mod, pos, cfg: BlockConfig,
     q = R(apply_rope(_split_heads(qkv[:, 0:d], cfg).transpose(1, 0, 2), pos, cfg)).transpose(1, 0, 2)
     k = R(apply_rope(_split_heads(qkv[:, d:2 * d], cfg).transpose(1, 0, 2), pos, cfg)).transpose(1, 0, 2)
     v = R(_split_heads(qkv[:, 2 * d:3 * d], cfg))
-    o = R(_merge_heads(attention(q, k, v)))
+    sel = slice(None) if rows is None else np.asarray(rows)
+    o = R(_merge_heads(attention(q, k, v, rows=rows)))
     oq, os_ = quantize_rows(o)
     a = R(linear_int8(oq, os_, w["q_o"], w["s_o"]))
-    x1 = R(x + gate1 * a)
+    x1 = R(x[sel] + gate1 * a)
     h2 = R(adaln(x1, shift2, scale2, cfg.eps))
     h2q, h2s = quantize_rows(h2)
     u = R(gelu_tanh(linear_int8(h2q, h2s, w["q1"], w["s1"])))

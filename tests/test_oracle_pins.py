@@ -455,3 +455,23 @@ def test_int8_block_close_to_float_block():
     # fc2 groups equal to F reduce to the per-token scheme
     a = O.block_forward_int8(x, wq, mod, pos, cfg, bf16_storage=False, fc2_group=128)
     assert np.linalg.norm((a - x) - (ref - x)) / np.linalg.norm(ref - x) < 3e-2
+
+
+def test_int8_block_rows_match_full_evaluation():
+    """Evaluating selected query rows gives those rows of the full block."""
+    cfg = O.BlockConfig(d=64, heads=2, head_dim=32, ffn=128, rope_sections=(8, 12, 12))
+    r = np.random.default_rng(16)
+    n = 20
+    wq = {}
+    for qn, sn, shp in (("q_qkv", "s_qkv", (192, 64)), ("q_o", "s_o", (64, 64)), ("q1", "s1", (128, 64)),
+                        ("q2", "s2", (64, 128))):
+        wq[qn], s = O.quantize_weight(r.standard_normal(shp) * 0.1)
+        wq[sn] = s[:, 0]
+    mod = r.standard_normal((6, 64)) * 0.3
+    x = r.standard_normal((n, 64))
+    pos = r.uniform(0, 5, (n, 3))
+    full = O.block_forward_int8(x, wq, mod, pos, cfg, bf16_storage=False, fc2_group=64)
+    rows = [0, 7, 19]
+    part = O.block_forward_int8(x, wq, mod, pos, cfg, bf16_storage=False, fc2_group=64, rows=rows)
+    assert np.allclose(part, full[rows], rtol=0, atol=1e-12)
+
