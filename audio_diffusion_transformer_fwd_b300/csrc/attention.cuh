@@ -1,29 +1,50 @@
 // Flash-style full attention on tcgen05 ([alphalab] model facts: the public
 // H3-Base runs full, non-causal attention over the joint sequence).
 //
-// One CTA owns 128 query rows of one head and walks all keys in tiles of 128:
-//   S_j   = Q K_j^T            tcgen05.mma into one of two TMEM S buffers
-//   P_j   = exp2(S_j * c - m)  4 softmax warps, one query row per thread,
-//                               written as BF16 into one of two shared P tiles
-//   O    += P_j V_j            tcgen05.mma accumulating in TMEM
-// with c = log2(e)/sqrt(Dh).  The running max m is only raised when a tile's
-// max exceeds it by more than 8 (a factor 256): then the row's O in TMEM and
-// its running sum are rescaled first.  Otherwise the stale max is kept; the
-// result is the same softmax because O and the sum use the same m.
+// One CTA owns 256 query rows of one head as two tiles of 128 (Q0, Q1) and
+// walks all keys in tiles of 128; both query tiles share every K/V tile it
+// loads.  Per key tile j and query tile i:
+//   S_i   = Q_i K_j^T           tcgen05.mma (both operands in shared memory)
+//                               into TMEM columns [128 i, 128 i + 128)
+//   P_i   = exp2(S_i * c - m_i) softmax warpgroup i (one query row per
+//                               thread), written back as BF16 into the first
+//                               64 columns of S_i's own TMEM
+//   O_i  += P_i V_j             tcgen05.mma with P_i read from TMEM
+// with c = log2(e)/sqrt(Dh).  The MMA thread alternates the two tiles, so
+// the tensor cores compute one tile's products while the other tile's
+// softmax runs.  The running max m_i is raised only when a tile's max
+// exceeds it by more than 8 (a factor 256): then the row's O in TMEM and its
+// running sum are rescaled first; otherwise the stale max is kept, which
+// gives the same softmax because O and the sum use the same m.
+//
+// Ordering through TMEM: S_i(j+1) overwrites the columns PV_i(j) reads P
+// from; both are issued by the one MMA thread in that order and tcgen05.mma
+// operations of a thread execute in issue order.  The completion of S_i(j)
+// (signalled by tcgen05.commit, which covers every earlier MMA of the
+// thread) also implies PV_i(j-1) is complete, so the softmax warpgroup may
+// rescale O_i as soon as S_i(j) has landed.
+//
+// exp2 is split between the MUFU unit and an FMA-pipe evaluation (one of
+// every four elements): x = n + f with n = rint(x), f in [-1/2, 1/2];
+// 2^f by a degree-3 polynomial (coefficients fitted here by iteratively
+// reweighted least squares for minimax relative error on [-1/2, 1/2]:
+// 1.0e-4 at most, far below the 2^-9 of P's BF16 rounding), and 2^n added
+// to the exponent field.  The two units then share the softmax's
+// exponentials.
 //
 // Operands are K-major BF16 in the 128-byte swizzle: Q and K come from the
 // head-major [H][N][Dh] tensors, V from its transpose [H][Dh][ld] written by
-// the QKV epilogue, and P is written by the softmax warps in the same
-// swizzled layout.  Keys past N read as zeros (TMA bounds) and are masked to
-// -inf; query rows past N are computed and not stored.
+// the QKV epilogue.  Keys past N read as zeros (TMA bounds) and are masked
+// to probability 0; query rows past N are computed and not stored.
 #pragma once
 #include "ptx.cuh"
 
 namespace h3 {
 
-constexpr int kAttnBQ = 128;
-constexpr int kAttnBKV = 128;
-constexpr int kAttnThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr int kAttnBQ = 128;        // rows of one query tile
+constexpr int kAttnTilesQ = 2;      // query tiles per CTA
+constexpr int kAttnBKV = 128;       // keys per tile
+constexpr int kAttnThreads = 384;   // warp 0 TMA, warp 1 MMA, warps 4-7 / 8-11 softmax
 constexpr float kAttnRescaleLog2 = 8.0f;
 
 template <int DH>
@@ -31,12 +52,10 @@ struct AttnSmem {
   static constexpr int kQBytes = kAttnBQ * DH * 2;
   static constexpr int kKBytes = kAttnBKV * DH * 2;
   static constexpr int kVBytes = DH * kAttnBKV * 2;
-  static constexpr int kPBytes = kAttnBQ * kAttnBKV * 2;
-  static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQOff + kQBytes;                 // 2 stages
+  static constexpr int kQOff = 0;                               // 2 query tiles
+  static constexpr int kKOff = kQOff + kAttnTilesQ * kQBytes;   // 2 stages
   static constexpr int kVOff = kKOff + 2 * kKBytes;             // 2 stages
-  static constexpr int kPOff = kVOff + 2 * kVBytes;             // 2 buffers
-  static constexpr int kBarOff = kPOff + 2 * kPBytes;
+  static constexpr int kBarOff = kVOff + 2 * kVBytes;
   static constexpr size_t kTotal = 1024 + kBarOff + 256;
 };
 
@@ -47,6 +66,34 @@ struct AttnArgs {
   float scale_log2;
 };
 
+// O_i (+)= P_i V: A operand (P, 128 rows x 16 keys per MMA) read from TMEM.
+__device__ __forceinline__ void tc_mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 2^x on the FMA pipe for x <= 64: rint by the 1.5 * 2^23 shifter, a
+// degree-3 polynomial for 2^f, f in [-1/2, 1/2], then n added to the
+// exponent.  x below -126 (including -inf) gives 0.
+__device__ __forceinline__ float exp2_fma(float x) {
+  const float xc = fmaxf(x, -126.0f);
+  const float t = xc + 12582912.0f;            // 1.5 * 2^23: rounds xc to an integer
+  const int n = __float_as_int(t);             // its low bits hold that integer
+  const float f = xc - (t - 12582912.0f);
+  float p = fmaf(f, 0.05500892922282219f, 0.24221095442771912f);
+  p = fmaf(p, f, 0.6932829022407532f);
+  p = fmaf(p, f, 1.0f);
+  const float r = __int_as_float(__float_as_int(p) + (n << 23));
+  return x < -126.0f ? 0.0f : r;
+}
+
 template <int DH>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -55,31 +102,33 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
-  // bars: q_full, kv_full[2], kv_empty[2], s_full[2], s_empty[2], p_full[2], pv_done[2], drain
+  // bars: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done[2], drain
   const uint32_t b_qfull = smem_u32(bars + 0);
-  const uint32_t b_kvfull = smem_u32(bars + 1);
-  const uint32_t b_kvempty = smem_u32(bars + 3);
-  const uint32_t b_sfull = smem_u32(bars + 5);
-  const uint32_t b_sempty = smem_u32(bars + 7);
-  const uint32_t b_pfull = smem_u32(bars + 9);
-  const uint32_t b_pvdone = smem_u32(bars + 11);
-  const uint32_t b_drain = smem_u32(bars + 13);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 14);
+  const uint32_t b_kfull = smem_u32(bars + 1);
+  const uint32_t b_kempty = smem_u32(bars + 3);
+  const uint32_t b_vfull = smem_u32(bars + 5);
+  const uint32_t b_vempty = smem_u32(bars + 7);
+  const uint32_t b_sfull = smem_u32(bars + 9);
+  const uint32_t b_pfull = smem_u32(bars + 11);
+  const uint32_t b_pvdone = smem_u32(bars + 13);
+  const uint32_t b_drain = smem_u32(bars + 15);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int q0 = blockIdx.x * kAttnBQ;
+  const int q0 = blockIdx.x * (kAttnTilesQ * kAttnBQ);
   const int head = blockIdx.y;
   const int nkv = (args.n + kAttnBKV - 1) / kAttnBKV;
 
   if (threadIdx.x == 0) {
     mbar_init(b_qfull, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(b_kvfull + 8 * i, 1);
-      mbar_init(b_kvempty + 8 * i, 1);
+      mbar_init(b_kfull + 8 * i, 1);
+      mbar_init(b_kempty + 8 * i, 1);
+      mbar_init(b_vfull + 8 * i, 1);
+      mbar_init(b_vempty + 8 * i, 1);
       mbar_init(b_sfull + 8 * i, 1);
-      mbar_init(b_sempty + 8 * i, 128);
       mbar_init(b_pfull + 8 * i, 128);
       mbar_init(b_pvdone + 8 * i, 1);
     }
@@ -95,9 +144,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  // TMEM columns: S buffers at 0 and 128, O at 256
-  const uint32_t t_s = tmem_base;
-  const uint32_t t_o = tmem_base + 256;
+  // TMEM columns: S_0 (and P_0) at 0, S_1 (and P_1) at 128, O_0 at 256, O_1 at 256 + DH
 
   if (warp == 0) {
     if (lane == 0) {
@@ -105,23 +152,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(b_qfull, L::kQBytes);
+      mbar_arrive_expect_tx(b_qfull, kAttnTilesQ * L::kQBytes);
 #pragma unroll
-      for (int a = 0; a < DH / 64; ++a)
-        tma_load_3d(smem_u32(smem + L::kQOff + a * kAttnBQ * 128), &tmQ, b_qfull, a * 64, q0, head);
-      for (int j = 0; j < nkv; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait(b_kvempty + 8 * st, ((j >> 1) & 1) ^ 1, abort_flag)) break;
-        const uint32_t fb = b_kvfull + 8 * st;
-        mbar_arrive_expect_tx(fb, L::kKBytes + L::kVBytes);
-        uint8_t* sk = smem + L::kKOff + st * L::kKBytes;
-        uint8_t* sv = smem + L::kVOff + st * L::kVBytes;
+      for (int i = 0; i < kAttnTilesQ; ++i)
 #pragma unroll
         for (int a = 0; a < DH / 64; ++a)
-          tma_load_3d(smem_u32(sk + a * kAttnBKV * 128), &tmK, fb, a * 64, j * kAttnBKV, head);
+          tma_load_3d(smem_u32(smem + L::kQOff + i * L::kQBytes + a * kAttnBQ * 128), &tmQ, b_qfull, a * 64,
+                      q0 + i * kAttnBQ, head);
+      int issued_k = 0, issued_v = 0;
+      bool ok = true;
+      for (int j = 0; j < nkv && ok; ++j) {
+        const int st = j & 1;
+        const uint32_t par = ((j >> 1) & 1) ^ 1;
+        if (!mbar_wait(b_kempty + 8 * st, par, abort_flag)) { ok = false; break; }
+        mbar_arrive_expect_tx(b_kfull + 8 * st, L::kKBytes);
+        uint8_t* sk = smem + L::kKOff + st * L::kKBytes;
+#pragma unroll
+        for (int a = 0; a < DH / 64; ++a)
+          tma_load_3d(smem_u32(sk + a * kAttnBKV * 128), &tmK, b_kfull + 8 * st, a * 64, j * kAttnBKV, head);
+        ++issued_k;
+        if (!mbar_wait(b_vempty + 8 * st, par, abort_flag)) { ok = false; break; }
+        mbar_arrive_expect_tx(b_vfull + 8 * st, L::kVBytes);
+        uint8_t* sv = smem + L::kVOff + st * L::kVBytes;
 #pragma unroll
         for (int a = 0; a < 2; ++a)
-          tma_load_3d(smem_u32(sv + a * DH * 128), &tmV, fb, j * kAttnBKV + a * 64, 0, head);
+          tma_load_3d(smem_u32(sv + a * DH * 128), &tmV, b_vfull + 8 * st, j * kAttnBKV + a * 64, 0, head);
+        ++issued_v;
+      }
+      if (!ok) {
+        // let the loads still in flight land before the CTA exits
+        for (int j = max(0, issued_k - 2); j < issued_k; ++j) mbar_wait_drain(b_kfull + 8 * (j & 1), (j >> 1) & 1);
+        for (int j = max(0, issued_v - 2); j < issued_v; ++j) mbar_wait_drain(b_vfull + 8 * (j & 1), (j >> 1) & 1);
+        mbar_wait_drain(b_qfull, 0);
       }
     }
   } else if (warp == 1) {
@@ -130,77 +192,102 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       constexpr uint32_t id_s = idesc_bf16_f32(kAttnBQ, kAttnBKV);
       constexpr uint32_t id_o = idesc_bf16_f32(kAttnBQ, DH);
       const uint32_t sq = smem_u32(smem + L::kQOff);
-      bool ok = mbar_wait(b_qfull, 0, abort_flag);
-      for (int j = 0; j <= nkv && ok; ++j) {
-        if (j < nkv) {
-          // S_j = Q K_j^T
-          const int st = j & 1;
-          if (!mbar_wait(b_kvfull + 8 * st, (j >> 1) & 1, abort_flag)) { ok = false; break; }
-          if (!mbar_wait(b_sempty + 8 * st, ((j >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t sk = smem_u32(smem + L::kKOff + st * L::kKBytes);
+      auto issue_s = [&](int i, int j) {
+        const uint32_t sk = smem_u32(smem + L::kKOff + (j & 1) * L::kKBytes);
+        const uint32_t sqi = sq + i * L::kQBytes;
 #pragma unroll
-          for (int kk = 0; kk < DH / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * (kAttnBQ * 128) + (kk & 3) * 32;
-            const uint32_t offk = (kk >> 2) * (kAttnBKV * 128) + (kk & 3) * 32;
-            tc_mma_bf16(t_s + st * kAttnBKV, sdesc_k128(sq + off), sdesc_k128(sk + offk), id_s, kk != 0);
-          }
-          tc_commit(b_sfull + 8 * st);
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (kAttnBQ * 128) + (kk & 3) * 32;
+          const uint32_t offk = (kk >> 2) * (kAttnBKV * 128) + (kk & 3) * 32;
+          tc_mma_bf16(tmem_base + i * kAttnBKV, sdesc_k128(sqi + off), sdesc_k128(sk + offk), id_s, kk != 0);
         }
-        if (j >= 1) {
-          // O += P_{j-1} V_{j-1}
-          const int jp = j - 1;
-          const int pb = jp & 1;
-          if (!mbar_wait(b_pfull + 8 * pb, (jp >> 1) & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t sp = smem_u32(smem + L::kPOff + pb * L::kPBytes);
-          const uint32_t sv = smem_u32(smem + L::kVOff + pb * L::kVBytes);
+        tc_commit(b_sfull + 8 * i);
+      };
+      auto issue_pv = [&](int i, int j) {
+        const uint32_t sv = smem_u32(smem + L::kVOff + (j & 1) * L::kVBytes);
 #pragma unroll
-          for (int kk = 0; kk < kAttnBKV / 16; ++kk) {
-            const uint32_t offp = (kk >> 2) * (kAttnBQ * 128) + (kk & 3) * 32;
-            const uint32_t offv = (kk >> 2) * (DH * 128) + (kk & 3) * 32;
-            tc_mma_bf16(t_o, sdesc_k128(sp + offp), sdesc_k128(sv + offv), id_o, (jp | kk) != 0);
-          }
-          tc_commit(b_kvempty + 8 * pb);
-          tc_commit(b_pvdone + 8 * pb);
+        for (int kk = 0; kk < kAttnBKV / 16; ++kk) {
+          const uint32_t offv = (kk >> 2) * (DH * 128) + (kk & 3) * 32;
+          tc_mma_bf16_ts(tmem_base + 256 + i * DH, tmem_base + i * kAttnBKV + kk * 8, sdesc_k128(sv + offv),
+                         id_o, (j | kk) != 0);
         }
+      };
+      bool ok = mbar_wait(b_qfull, 0, abort_flag) && mbar_wait(b_kfull, 0, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        issue_s(1, 0);
+        tc_commit(b_kempty);
+      }
+      for (int j = 0; j < nkv && ok; ++j) {
+        const int st = j & 1;
+        const uint32_t par = (j >> 1) & 1;
+        const bool more = j + 1 < nkv;
+        if (!mbar_wait(b_vfull + 8 * st, par, abort_flag)) { ok = false; break; }
+        // tile 0: O_0 += P_0 V_j, then S_0 of the next key tile
+        if (!mbar_wait(b_pfull, j & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        issue_pv(0, j);
+        if (more) {
+          if (!mbar_wait(b_kfull + 8 * ((j + 1) & 1), ((j + 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(0, j + 1);
+        }
+        // tile 1
+        if (!mbar_wait(b_pfull + 8, j & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        issue_pv(1, j);
+        tc_commit(b_vempty + 8 * st);
+        if (more) {
+          issue_s(1, j + 1);
+          tc_commit(b_kempty + 8 * ((j + 1) & 1));
+        }
+      }
+      if (ok) {
+        tc_commit(b_pvdone);
+        tc_commit(b_pvdone + 8);
       }
       tc_commit(b_drain);
       mbar_wait_drain(b_drain, 0);
     }
-  } else {
-    // ---------------- softmax / correction warps 2..5
+  } else if (warp >= 4) {
+    // ---------------- softmax warpgroups: warps 4-7 query tile 0, 8-11 tile 1
+    const int ti = (warp - 4) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t t_s = tmem_base + lane_off + ti * kAttnBKV;
+    const uint32_t t_o = tmem_base + lane_off + 256 + ti * DH;
+    const uint32_t b_s = b_sfull + 8 * ti;
+    const uint32_t b_p = b_pfull + 8 * ti;
     const float c = args.scale_log2;
     float m_eff = -INFINITY;
     float l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
-      const int st = j & 1;
-      if (!mbar_wait(b_sfull + 8 * st, (j >> 1) & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait(b_s, j & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
       float s[kAttnBKV];
 #pragma unroll
       for (int cc = 0; cc < kAttnBKV / 32; ++cc) {
         float v[32];
-        tmem_ld32(t_s + lane_off + st * kAttnBKV + cc * 32, v);
+        tmem_ld32(t_s + cc * 32, v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[cc * 32 + i] = v[i];
       }
-      tc_fence_before();
-      mbar_arrive(b_sempty + 8 * st);
       const int valid = args.n - j * kAttnBKV;
       if (valid < kAttnBKV) {
 #pragma unroll
         for (int i = 0; i < kAttnBKV; ++i)
           if (i >= valid) s[i] = -INFINITY;
       }
-      float mx = -INFINITY;
+      float mx4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-      for (int i = 0; i < kAttnBKV; ++i) mx = fmaxf(mx, s[i]);
-      mx *= c;
+      for (int i = 4; i < kAttnBKV; i += 4) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) mx4[e] = fmaxf(mx4[e], s[i + e]);
+      }
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c;
       float alpha = 1.f;
       bool rescale = false;
       if (j == 0) {
@@ -210,61 +297,49 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         m_eff = mx;
         rescale = true;
       }
-      l *= alpha;
-      // P_j -> shared buffer j&1 (its previous reader PV_{j-2} finished:
-      // waited for below at iteration j-1)
-      const int pb = j & 1;
-      uint8_t* sp = smem + L::kPOff + pb * L::kPBytes;
-      float sum = 0.f;
+      const float neg_m = -m_eff;
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int ch = 0; ch < kAttnBKV / 8; ++ch) {
-        uint32_t pk[4];
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = fast_exp2(fmaf(s[ch * 8 + 2 * e], c, -m_eff));
-          const float p1 = fast_exp2(fmaf(s[ch * 8 + 2 * e + 1], c, -m_eff));
-          sum += p0 + p1;
+        for (int e = 0; e < 32; ++e) {
+          const int i = half * 64 + 2 * e;
+          const float x0 = fmaf(s[i], c, neg_m);
+          const float x1 = fmaf(s[i + 1], c, neg_m);
+          const float p0 = fast_exp2(x0);
+          const float p1 = (e & 1) ? exp2_fma(x1) : fast_exp2(x1);
+          sum4[e & 3] += p0 + p1;
           pk[e] = pack_bf16x2(p0, p1);
         }
-        // 128-byte swizzle: 16-byte chunk (ch % 8) of row `row` in atom ch / 8
-        const int atom = ch >> 3;
-        const int chunk = (ch & 7) ^ (row & 7);
-        *reinterpret_cast<uint4*>(sp + atom * (kAttnBQ * 128) + row * 128 + chunk * 16) =
-            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        tmem_st32u(t_s + half * 32, pk);
       }
-      l += sum;
-      // PV_{j-1} must be complete before O is rescaled, and before P buffer
-      // (j+1)&1 is overwritten at the next iteration.
-      if (j >= 1) {
-        const int jp = j - 1;
-        if (!mbar_wait(b_pvdone + 8 * (jp & 1), (jp >> 1) & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, rescale)) {
+      l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+      // O_i holds the products up to key tile j-1 (complete: S_i(j) was
+      // issued after them); rescale it to the new max before PV_i(j).
+      if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-          for (int cc = 0; cc < DH / 32; ++cc) {
-            float v[32];
-            tmem_ld32(t_o + lane_off + cc * 32, v);
+        for (int cc = 0; cc < DH / 32; ++cc) {
+          float v[32];
+          tmem_ld32(t_o + cc * 32, v);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= alpha;
-            tmem_st32(t_o + lane_off + cc * 32, v);
-          }
+          for (int i = 0; i < 32; ++i) v[i] *= alpha;
+          tmem_st32(t_o + cc * 32, v);
         }
       }
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(b_pfull + 8 * pb);
+      mbar_arrive(b_p);
     }
     if (ok) {
-      const int jl = nkv - 1;
-      if (mbar_wait(b_pvdone + 8 * (jl & 1), (jl >> 1) & 1, abort_flag)) {
+      if (mbar_wait(b_pvdone + 8 * ti, 0, abort_flag)) {
         tc_fence_after();
-        const int grow = q0 + row;
+        const int grow = q0 + ti * kAttnBQ + row;
         const float inv = 1.f / l;
         const int d = args.heads * DH;
 #pragma unroll 1
         for (int cc = 0; cc < DH / 32; ++cc) {
           float v[32];
-          tmem_ld32(t_o + lane_off + cc * 32, v);
+          tmem_ld32(t_o + cc * 32, v);
           if (grow < args.n) {
             uint32_t p[16];
 #pragma unroll

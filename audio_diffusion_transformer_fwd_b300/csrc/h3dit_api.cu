@@ -341,7 +341,8 @@ h3dit_status launch_attention(const h3dit_config* c, const void* q, const void* 
   a.heads = H;
   a.o = static_cast<bf16*>(o);
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)dh);
-  dim3 grid((n + h3::kAttnBQ - 1) / h3::kAttnBQ, H);
+  const int rows_per_cta = h3::kAttnTilesQ * h3::kAttnBQ;
+  dim3 grid((n + rows_per_cta - 1) / rows_per_cta, H);
   TimedLaunch tl(kAttn, s);
   if (dh == 128) {
     static bool once = false;
