@@ -24,13 +24,10 @@
 // thread) also implies PV_i(j-1) is complete, so the softmax warpgroup may
 // rescale O_i as soon as S_i(j) has landed.
 //
-// exp2 is split between the MUFU unit and an FMA-pipe evaluation (one of
-// every four elements): x = n + f with n = rint(x), f in [-1/2, 1/2];
-// 2^f by a degree-3 polynomial (coefficients fitted here by iteratively
-// reweighted least squares for minimax relative error on [-1/2, 1/2]:
-// 1.0e-4 at most, far below the 2^-9 of P's BF16 rounding), and 2^n added
-// to the exponent field.  The two units then share the softmax's
-// exponentials.
+// The softmax of a row costs about 2 instructions per score: one 128-column
+// TMEM load, 3-input max, packed (f32x2) scale-and-subtract and sums, MUFU
+// exp2 (its rate on this part keeps it off the critical path), one BF16
+// pack per pair and two TMEM stores.
 //
 // Operands are K-major BF16 in the 128-byte swizzle: Q and K come from the
 // head-major [H][N][Dh] tensors, V from its transpose [H][Dh][ld] written by
@@ -77,21 +74,6 @@ __device__ __forceinline__ void tc_mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem,
       "}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
-}
-
-// 2^x on the FMA pipe for x <= 64: rint by the 1.5 * 2^23 shifter, a
-// degree-3 polynomial for 2^f, f in [-1/2, 1/2], then n added to the
-// exponent.  x below -126 (including -inf) gives 0.
-__device__ __forceinline__ float exp2_fma(float x) {
-  const float xc = fmaxf(x, -126.0f);
-  const float t = xc + 12582912.0f;            // 1.5 * 2^23: rounds xc to an integer
-  const int n = __float_as_int(t);             // its low bits hold that integer
-  const float f = xc - (t - 12582912.0f);
-  float p = fmaf(f, 0.05500892922282219f, 0.24221095442771912f);
-  p = fmaf(p, f, 0.6932829022407532f);
-  p = fmaf(p, f, 1.0f);
-  const float r = __int_as_float(__float_as_int(p) + (n << 23));
-  return x < -126.0f ? 0.0f : r;
 }
 
 template <int DH>
@@ -268,13 +250,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (!mbar_wait(b_s, j & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
       float s[kAttnBKV];
-#pragma unroll
-      for (int cc = 0; cc < kAttnBKV / 32; ++cc) {
-        float v[32];
-        tmem_ld32(t_s + cc * 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[cc * 32 + i] = v[i];
-      }
+      tmem_ld128(t_s, s);
       const int valid = args.n - j * kAttnBKV;
       if (valid < kAttnBKV) {
 #pragma unroll
@@ -283,11 +259,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       float mx4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-      for (int i = 4; i < kAttnBKV; i += 4) {
+      for (int i = 4; i < kAttnBKV - 4; i += 8) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) mx4[e] = fmaxf(mx4[e], s[i + e]);
+        for (int e = 0; e < 4; ++e) mx4[e] = fmax3(mx4[e], s[i + 2 * e], s[i + 2 * e + 1]);
       }
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c;
+      const float mx = fmax3(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]),
+                             fmax3(s[kAttnBKV - 4], s[kAttnBKV - 3], fmaxf(s[kAttnBKV - 2], s[kAttnBKV - 1]))) * c;
       float alpha = 1.f;
       bool rescale = false;
       if (j == 0) {
@@ -298,23 +275,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         rescale = true;
       }
       const float neg_m = -m_eff;
-      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // 4 packed partial sums
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int i = half * 64 + 2 * e;
-          const float x0 = fmaf(s[i], c, neg_m);
-          const float x1 = fmaf(s[i + 1], c, neg_m);
+          float x0, x1;
+          ffma2(x0, x1, s[i], s[i + 1], c, c, neg_m, neg_m);
           const float p0 = fast_exp2(x0);
-          const float p1 = (e & 1) ? exp2_fma(x1) : fast_exp2(x1);
-          sum4[e & 3] += p0 + p1;
+          const float p1 = fast_exp2(x1);
+          const int a = 2 * (e & 3);
+          fadd2(acc[a], acc[a + 1], acc[a], acc[a + 1], p0, p1);
           pk[e] = pack_bf16x2(p0, p1);
         }
         tmem_st32u(t_s + half * 32, pk);
       }
-      l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+      l = l * alpha + (((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7])));
       // O_i holds the products up to key tile j-1 (complete: S_i(j) was
       // issued after them); rescale it to the new max before PV_i(j).
       if (__any_sync(0xffffffffu, rescale)) {
