@@ -366,6 +366,21 @@ bool fusion_disabled() {
   return v == 1;
 }
 
+template <bool GATE, bool NORM, bool QUANT>
+void launch_row_kernel(int nv, bf16* x, const bf16* branch, const float* gate, const float* shift,
+                       const float* scale, bf16* h, float* hs, int n, int d, float eps, cudaStream_t s) {
+#define H3_ROW_CASE(NVV)                                                                               \
+  case NVV:                                                                                            \
+    h3::gate_adaln_kernel<GATE, NORM, QUANT, NVV><<<n, h3::kRowThreads, 0, s>>>(x, branch, gate, shift, \
+                                                                                 scale, h, hs, d, eps); \
+    break;
+  switch (nv) {
+    H3_ROW_CASE(1) H3_ROW_CASE(2) H3_ROW_CASE(3) H3_ROW_CASE(4)
+    H3_ROW_CASE(5) H3_ROW_CASE(6) H3_ROW_CASE(7) default: H3_ROW_CASE(8)
+  }
+#undef H3_ROW_CASE
+}
+
 // Gated residual (branch != NULL) and/or AdaLN (shift != NULL).  hs != NULL
 // selects the int8 form of the AdaLN output: h receives the row's int8 codes
 // as BF16 values and hs[row] the scale.
@@ -378,22 +393,22 @@ h3dit_status launch_rows(void* x, const void* branch, const float* gate, const f
   const bool gate_on = branch != nullptr;
   const bool norm_on = shift != nullptr;
   const bool quant = hs != nullptr;
+  if (d % 8 != 0 || d > h3::kRowMaxVec * h3::kRowThreads * 8)
+    return fail(H3DIT_E_UNSUPPORTED, "row width %d (multiple of 8, <= 8192)", d);
+  const int nv = (d / 8 + h3::kRowThreads - 1) / h3::kRowThreads;
   if (gate_on && norm_on && !fusion_disabled()) {
     if (quant)
-      h3::gate_adaln_kernel<true, true, true><<<n, h3::kRowThreads, 0, s>>>(xb, bb, gate, shift, scale, hb, hs, d, eps);
+      launch_row_kernel<true, true, true>(nv, xb, bb, gate, shift, scale, hb, hs, n, d, eps, s);
     else
-      h3::gate_adaln_kernel<true, true><<<n, h3::kRowThreads, 0, s>>>(xb, bb, gate, shift, scale, hb, nullptr, d, eps);
+      launch_row_kernel<true, true, false>(nv, xb, bb, gate, shift, scale, hb, nullptr, n, d, eps, s);
   } else {
     if (gate_on)
-      h3::gate_adaln_kernel<true, false><<<n, h3::kRowThreads, 0, s>>>(xb, bb, gate, nullptr, nullptr, nullptr,
-                                                                       nullptr, d, eps);
+      launch_row_kernel<true, false, false>(nv, xb, bb, gate, nullptr, nullptr, nullptr, nullptr, n, d, eps, s);
     if (norm_on) {
       if (quant)
-        h3::gate_adaln_kernel<false, true, true><<<n, h3::kRowThreads, 0, s>>>(xb, nullptr, nullptr, shift, scale, hb,
-                                                                               hs, d, eps);
+        launch_row_kernel<false, true, true>(nv, xb, nullptr, nullptr, shift, scale, hb, hs, n, d, eps, s);
       else
-        h3::gate_adaln_kernel<false, true><<<n, h3::kRowThreads, 0, s>>>(xb, nullptr, nullptr, shift, scale, hb,
-                                                                         nullptr, d, eps);
+        launch_row_kernel<false, true, false>(nv, xb, nullptr, nullptr, shift, scale, hb, nullptr, n, d, eps, s);
     }
   }
   H3_CUDA(cudaGetLastError());

@@ -50,8 +50,15 @@ __device__ __forceinline__ int quant_code(float x, float s) {
 // int8 codes of bf16(h) at s = absmax(bf16(h)) / 127 are written into h as
 // BF16 values, and s into hs[row] -- the same codes h3dit_quantize_act gives
 // for the BF16 h.
-template <bool GATE, bool NORM, bool QUANT = false>
-__global__ void __launch_bounds__(kRowThreads)
+// NV = ceil(d / (8 * 128)) 16-byte vectors per thread: the row's register
+// copy is sized to the actual width.  The kernel is latency-bound on its two
+// block reductions, so resident rows per SM set its bandwidth: up to NV = 5
+// (d <= 5120) the registers are capped for 8 CTAs per SM.
+template <int NV>
+constexpr int row_min_blocks() { return NV <= 5 ? 8 : 5; }
+
+template <bool GATE, bool NORM, bool QUANT, int NV>
+__global__ void __launch_bounds__(kRowThreads, row_min_blocks<NV>())
     gate_adaln_kernel(__nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ branch,
                       const float* __restrict__ gate, const float* __restrict__ shift,
                       const float* __restrict__ scale, __nv_bfloat16* __restrict__ h,
@@ -61,10 +68,10 @@ __global__ void __launch_bounds__(kRowThreads)
   const int nvec = d >> 3;
   uint4* xr = reinterpret_cast<uint4*>(x + row * d);
   const uint4* br = reinterpret_cast<const uint4*>(branch + (GATE ? row * d : 0));
-  float v[kRowMaxVec][8];
+  float v[NV][8];
   float sum = 0.f;
 #pragma unroll
-  for (int i = 0; i < kRowMaxVec; ++i) {
+  for (int i = 0; i < NV; ++i) {
     const int idx = i * kRowThreads + threadIdx.x;
     if (idx < nvec) {
       unpack8(xr[idx], v[i]);
@@ -88,7 +95,7 @@ __global__ void __launch_bounds__(kRowThreads)
   const float mean = block_sum_128(sum, red) / static_cast<float>(d);
   float sq = 0.f;
 #pragma unroll
-  for (int i = 0; i < kRowMaxVec; ++i) {
+  for (int i = 0; i < NV; ++i) {
     const int idx = i * kRowThreads + threadIdx.x;
     if (idx < nvec) {
 #pragma unroll
@@ -102,7 +109,7 @@ __global__ void __launch_bounds__(kRowThreads)
   const float rstd = rsqrtf(var + eps);
   uint4* hr = reinterpret_cast<uint4*>(h + row * d);
 #pragma unroll
-  for (int i = 0; i < kRowMaxVec; ++i) {
+  for (int i = 0; i < NV; ++i) {
     const int idx = i * kRowThreads + threadIdx.x;
     if (idx < nvec) {
       const float4 s0 = __ldg(reinterpret_cast<const float4*>(scale) + 2 * idx);
@@ -124,7 +131,7 @@ __global__ void __launch_bounds__(kRowThreads)
   if (!QUANT) return;
   float amax = 0.f;
 #pragma unroll
-  for (int i = 0; i < kRowMaxVec; ++i) {
+  for (int i = 0; i < NV; ++i) {
     const int idx = i * kRowThreads + threadIdx.x;
     if (idx < nvec) {
 #pragma unroll
@@ -140,7 +147,7 @@ __global__ void __launch_bounds__(kRowThreads)
   const float sq8 = __fdiv_rn(amax, 127.0f);
   if (threadIdx.x == 0) hs[row] = sq8;
 #pragma unroll
-  for (int i = 0; i < kRowMaxVec; ++i) {
+  for (int i = 0; i < NV; ++i) {
     const int idx = i * kRowThreads + threadIdx.x;
     if (idx < nvec) {
       float c[8];

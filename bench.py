@@ -301,12 +301,19 @@ def run_ours(args):
         "fc2_gemm": {"ms": per_class["fc2"][0] / args.steps, "tflops": 2.0 * n * d * f / (per_class["fc2"][0] / args.steps * 1e-3) / 1e12},
         "attention": {"ms": attn_ms, "tflops": 4.0 * n * n * d / (attn_ms * 1e-3) / 1e12,
                       "frac_of_burst": 4.0 * n * n * d / (attn_ms * 1e-3) / 1e12 / burst},
-        "row_kernels": {"ms": rows_ms, "note": "rope table + AdaLN + 2 gated residual/AdaLN per block"},
+        "row_kernels": {"ms": rows_ms, "note": "rope table + AdaLN-1 + gated residual fused with AdaLN-2 + "
+                        "final gated residual per block"},
     }
-    # two gated-residual+AdaLN rows per block: read x, branch; write x, h (8 N d bytes each)
+    # algorithmic bytes of the row kernels of one block: AdaLN-1 reads x and
+    # writes h (4 N d), the fused gated residual + AdaLN-2 reads x and the
+    # branch and writes x and h2 (8 N d), the final gated residual reads x and
+    # the branch and writes x (6 N d); the RoPE table reads the positions and
+    # writes N * Dh/2 (cos, sin) fp32 pairs
+    rows_bytes = 18.0 * n * d + n * (12.0 + (w.head_dim // 2) * 8.0)
     rows_gbs = None
     if rows_ms > 0:
-        rows_gbs = (2 * 8.0 * n * d + 4.0 * n * d) / (rows_ms * 1e-3) / 1e9
+        rows_gbs = rows_bytes / (rows_ms * 1e-3) / 1e9
+        kernels["row_kernels"]["bytes_per_block"] = rows_bytes
         kernels["row_kernels"]["gbs"] = rows_gbs
         kernels["row_kernels"]["frac_of_hbm"] = rows_gbs / hbm
 
