@@ -80,6 +80,42 @@ def ncu_traffic(kernel_key):
     return j.get("kernels", {}).get(kernel_key)
 
 
+def write_traffic(csv_path):
+    """profiles/ncu_traffic.json from an ncu --csv capture of
+    dram__bytes_read.sum and dram__bytes_write.sum over the launches of one
+    block (the command is in profiles/dram_traffic_block_512.md): DRAM bytes
+    per launch by kernel class, and the four GEMM launches' sum, stamped with
+    the hash of the kernel sources they were taken on."""
+    import csv
+    import re
+    scale = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1024.0, "MB": 1024.0 ** 2}
+    with open(csv_path) as fh:
+        rows = [r for r in csv.reader(fh)]
+    hi = next(i for i, r in enumerate(rows) if r and r[0] == "ID")
+    hdr = rows[hi]
+    ki, mi, vi, ui = (hdr.index(c) for c in ("Kernel Name", "Metric Name", "Metric Value", "Metric Unit"))
+    per_launch = {}
+    for r in rows[hi + 1:]:
+        if r[mi] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        per_launch.setdefault(r[0], [r[ki], 0.0])[1] += float(r[vi].replace(",", "")) * scale.get(r[ui], 1.0)
+    order = ["qkv_gemm", "out_proj_gemm", "fc1_gemm", "fc2_gemm"]
+    gemms = [(name, b) for name, b in per_launch.values() if "gemm" in name]
+    out = {"source_hash": kernel_source_hash(), "unit": "bytes per launch", "kernels": {}}
+    for key, (name, b) in zip(order, gemms[:4]):
+        out["kernels"][key] = b
+    if len(gemms) >= 4:
+        out["kernels"]["gemm_per_block"] = sum(b for _, b in gemms[:4])
+    for name, b in per_launch.values():
+        m = re.search(r"(attn_fwd|gate_adaln_kernel<[^>]*>|rope_table)", name)
+        if m:
+            out["kernels"].setdefault(m.group(1), b)
+    with open(os.path.join(ROOT, "profiles", "ncu_traffic.json"), "w") as fh:
+        json.dump(out, fh, indent=1)
+    print(json.dumps(out))
+    return 0
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled during the timed region."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -490,6 +526,48 @@ def run_steps(args, H, synth, torch, stream, barrier, max_over_ranks, rank):
     return out
 
 
+def run_profile(args):
+    """The 512-class block, BF16 or int8, run warmup + steps times with no
+    timing: a short, fixed launch sequence for ncu (one block = rope table,
+    AdaLN, QKV GEMM, attention, out-proj GEMM, fused residual + AdaLN, FC1,
+    FC2, residual; int8 adds the quantisers)."""
+    import torch
+    from audio_diffusion_transformer_fwd_b300 import h3dit as H
+    from audio_diffusion_transformer_fwd_b300 import synth
+    torch.cuda.set_device(0)
+    w = synth.WORKLOADS["block_512"]
+    n, d, f = w.n_tokens, w.d, w.ffn
+    if args.tokens:
+        n = max(1, min(n, args.tokens))
+    prec = H.INT8 if args.profile == "int8" else H.BF16
+    shape = H.BlockShape(w.d, w.heads, w.head_dim, w.ffn, w.eps, w.sections, w.theta, prec)
+    wdev = synth.device_block_weights(d, f, seed=0, block=0)
+    if prec == H.INT8:
+        codes, scales = {}, {}
+        for k, t in wdev.items():
+            q8 = torch.empty(t.shape, device="cuda", dtype=torch.int8)
+            sc = torch.empty(t.shape[0], device="cuda", dtype=torch.float32)
+            H.h3dit_quantize_weight(t, t.shape[0], t.shape[1], q8, sc)
+            cb = torch.empty(t.shape, device="cuda", dtype=torch.bfloat16)
+            H.h3dit_widen_codes(q8, q8.numel(), cb)
+            codes[k], scales[k] = cb, sc
+        bw = H.block_weights(codes["w_qkv"], codes["w_o"], codes["w1"], codes["w2"],
+                             scales["w_qkv"], scales["w_o"], scales["w1"], scales["w2"])
+    else:
+        bw = H.block_weights(wdev["w_qkv"], wdev["w_o"], wdev["w1"], wdev["w2"])
+    mod = synth.device_mods(1, d, seed=0)
+    x = synth.device_activations(n, d, seed=0)
+    pos = torch.from_numpy(synth.positions(w.video, w.n_text, w.n_audio)[:n]).cuda()
+    nbytes = H.h3dit_workspace_size(shape, n)
+    wsb = torch.empty(nbytes, device="cuda", dtype=torch.uint8)
+    for _ in range(args.warmup + args.steps):
+        H.h3dit_block_forward(shape, bw, mod, x, pos, n, wsb, nbytes)
+    H.h3dit_check_device_error()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": args.profile, "tokens": n, "blocks": args.warmup + args.steps}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -498,9 +576,20 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-step", action="store_true", help="omit the 50-block step latencies")
     ap.add_argument("--skip-cpu", action="store_true", help="omit the oracle CPU baseline")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="with --profile: run the block on the first TOKENS tokens of the workload (a small case)")
+    ap.add_argument("--profile", choices=["bf16", "int8"], default=None,
+                    help="run only WARMUP + STEPS forwards of the 512-class block (no report): the command "
+                         "the ncu captures under profiles/ run")
+    ap.add_argument("--traffic-from", default=None,
+                    help="write profiles/ncu_traffic.json from an ncu DRAM-bytes CSV of one block and exit")
     args = ap.parse_args()
+    if args.traffic_from:
+        return write_traffic(args.traffic_from)
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile:
+        return run_profile(args)
     return run_ours(args)
 
 
