@@ -134,6 +134,23 @@ h3dit_status make_map(CUtensorMap* m, const void* base, int rank, const uint64_t
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Which projections run on int8 codes ([linlog] "int8 量化": the MLP alone,
+// QKV alone, or all four).
+struct Int8Set {
+  bool qkv = false, o = false, fc1 = false, fc2 = false;
+  bool any() const { return qkv || o || fc1 || fc2; }
+};
+Int8Set int8_set(int precision) {
+  Int8Set q;
+  switch (precision) {
+    case H3DIT_INT8: q.qkv = q.o = q.fc1 = q.fc2 = true; break;
+    case H3DIT_INT8_MLP: q.fc1 = q.fc2 = true; break;
+    case H3DIT_INT8_QKV: q.qkv = true; break;
+    default: break;
+  }
+  return q;
+}
+
 // ------------------------------------------------------------------ config checks
 h3dit_status check_cfg(const h3dit_config* c) {
   if (!c) return fail(H3DIT_E_INVAL, "config is NULL");
@@ -153,9 +170,9 @@ h3dit_status check_cfg(const h3dit_config* c) {
   if (s != c->head_dim) return fail(H3DIT_E_INVAL, "rope sections sum %d != head_dim %d", s, c->head_dim);
   if (!(c->eps > 0.f)) return fail(H3DIT_E_INVAL, "eps must be > 0");
   if (!(c->rope_theta > 0.f)) return fail(H3DIT_E_INVAL, "rope_theta must be > 0");
-  if (c->precision != H3DIT_BF16 && c->precision != H3DIT_INT8)
+  if (c->precision < H3DIT_BF16 || c->precision > H3DIT_INT8_QKV)
     return fail(H3DIT_E_INVAL, "precision %d", c->precision);
-  if (c->precision == H3DIT_INT8 && c->ffn > 1024 && c->ffn % 1024 != 0)
+  if (int8_set(c->precision).fc2 && c->ffn > 1024 && c->ffn % 1024 != 0)
     return fail(H3DIT_E_UNSUPPORTED, "int8 ffn %d (FC2 scale groups of 1024 need ffn <= 1024 or a multiple of 1024)",
                 c->ffn);
   return H3DIT_OK;
@@ -474,7 +491,7 @@ Arena plan_arena(const h3dit_config* c, int n, const h3dit_reduction* tr) {
   a.a2 = off; off += nd;
   a.a3 = off; off += nd;
   a.rope = off; off += round_up((size_t)n * (c->head_dim / 2) * 8, 256);
-  if (c->precision == H3DIT_INT8) {
+  if (int8_set(c->precision).any()) {
     a.sc_row = off; off += round_up((size_t)n * 4, 256);
     a.sc_grp = off; off += round_up((size_t)n * (F / fc2_group(c)) * 4, 256);
   }
@@ -493,20 +510,24 @@ struct BlockBufs {
   Arena ar;
 };
 
-// The dynamic-int8 block body ([linlog] "int8 量化"): QKV, out-projection
-// and FC1 take per-token int8 codes, FC2 per-token codes with one scale per
-// 1024 input channels; weights are per-output-channel int8 codes.  Attention
-// stays BF16.  Entry: a2 holds the AdaLN-1 codes and sc_row their scales.
-h3dit_status run_block_body_i8(const h3dit_config* c, const h3dit_block_weights* w, const float* mod, bf16* x,
-                               int n, const float* rope, const BlockBufs& B, int vt_ld,
-                               const float* next_shift, const float* next_scale, cudaStream_t s) {
+// One block's sub-steps from its AdaLN-1 output (already in a2) to the final
+// gated residual.  Projections in `q8` run on int8 codes ([linlog] "int8
+// 量化"): their input is quantised per token (FC2's per token and per 1024
+// channels) and a2 then holds codes, with the scales in sc_row / sc_grp;
+// the others run in BF16.  Attention stays BF16.  next_shift/next_scale: the
+// following block's AdaLN-1 vectors to emit into a2 from the residual
+// kernel (as codes if that block's QKV is int8), or NULL.
+h3dit_status run_block_body(const h3dit_config* c, const h3dit_block_weights* w, const float* mod, bf16* x,
+                            int n, const float* rope, const BlockBufs& B, int vt_ld,
+                            const float* next_shift, const float* next_scale, cudaStream_t s) {
   const int d = c->d, F = c->ffn, dh = c->head_dim;
+  const Int8Set q8 = int8_set(c->precision);
   const int g2 = fc2_group(c);
   uint8_t* a1 = B.base + B.ar.a1;
   bf16* a2 = reinterpret_cast<bf16*>(B.base + B.ar.a2);
   bf16* a3 = reinterpret_cast<bf16*>(B.base + B.ar.a3);
-  float* sc_row = reinterpret_cast<float*>(B.base + B.ar.sc_row);
-  float* sc_grp = reinterpret_cast<float*>(B.base + B.ar.sc_grp);
+  float* sc_row = q8.any() ? reinterpret_cast<float*>(B.base + B.ar.sc_row) : nullptr;
+  float* sc_grp = q8.any() ? reinterpret_cast<float*>(B.base + B.ar.sc_grp) : nullptr;
   bf16* q = reinterpret_cast<bf16*>(a1);
   bf16* k = reinterpret_cast<bf16*>(a1 + round_up((size_t)n * d * 2, 256));
   bf16* vt = reinterpret_cast<bf16*>(a1 + 2 * round_up((size_t)n * d * 2, 256));
@@ -519,71 +540,47 @@ h3dit_status run_block_body_i8(const h3dit_config* c, const h3dit_block_weights*
   h3::GemmArgs g{};
   g.q = q; g.k = k; g.vt = vt; g.vt_ld = vt_ld; g.d = d; g.head_dim = dh;
   g.rope = reinterpret_cast<const float2*>(rope);
-  H3_TRY(launch_gemm_i8(h3::kEpiQKV, a2, sc_row, d, w->w_qkv, w->s_qkv, n, 3 * d, d, g, nullptr, kQKV, s));
-  H3_TRY(launch_attention(c, q, k, vt, vt_ld, n, a3, s));
-  H3_TRY(launch_quantize_codes(a3, n, d, d, a2, sc_row, s));
+  if (q8.qkv)
+    H3_TRY(launch_gemm_i8(h3::kEpiQKV, a2, sc_row, d, w->w_qkv, w->s_qkv, n, 3 * d, d, g, nullptr, kQKV, s));
+  else
+    H3_TRY(launch_gemm(h3::kEpiQKV, a2, w->w_qkv, n, 3 * d, d, g, kQKV, s));
   h3::GemmArgs go{};
   go.c = a3; go.ldc = d;
-  H3_TRY(launch_gemm_i8(h3::kEpiStore, a2, sc_row, d, w->w_o, w->s_o, n, d, d, go, nullptr, kOProj, s));
-  H3_TRY(launch_rows(x, a3, gate1, shift2, scale2, a2, sc_row, n, d, c->eps, s));
+  if (q8.o) {
+    // o into a3, its codes into a2 (h is dead), the projection back into a3
+    H3_TRY(launch_attention(c, q, k, vt, vt_ld, n, a3, s));
+    H3_TRY(launch_quantize_codes(a3, n, d, d, a2, sc_row, s));
+    H3_TRY(launch_gemm_i8(h3::kEpiStore, a2, sc_row, d, w->w_o, w->s_o, n, d, d, go, nullptr, kOProj, s));
+  } else {
+    H3_TRY(launch_attention(c, q, k, vt, vt_ld, n, a2, s));
+    H3_TRY(launch_gemm(h3::kEpiStore, a2, w->w_o, n, d, d, go, kOProj, s));
+  }
+  H3_TRY(launch_rows(x, a3, gate1, shift2, scale2, a2, q8.fc1 ? sc_row : nullptr, n, d, c->eps, s));
   h3::GemmArgs g1{};
   g1.c = u; g1.ldc = F;
-  H3_TRY(launch_gemm_i8(h3::kEpiGelu, a2, sc_row, d, w->w1, w->s1, n, F, d, g1, nullptr, kFC1, s));
-  H3_TRY(launch_quantize_codes(u, n, F, g2, u, sc_grp, s));
+  if (q8.fc1)
+    H3_TRY(launch_gemm_i8(h3::kEpiGelu, a2, sc_row, d, w->w1, w->s1, n, F, d, g1, nullptr, kFC1, s));
+  else
+    H3_TRY(launch_gemm(h3::kEpiGelu, a2, w->w1, n, F, d, g1, kFC1, s));
   h3::GemmArgs gm{};
   gm.c = a3; gm.ldc = d;
-  H3_TRY(launch_gemm_i8(h3::kEpiStore, u, sc_grp, g2, w->w2, w->s2, n, d, F, gm, nullptr, kFC2, s));
-  H3_TRY(launch_rows(x, a3, gate2, next_shift, next_scale, a2, next_shift ? sc_row : nullptr, n, d, c->eps, s));
-  return H3DIT_OK;
-}
-
-// Runs one block's sub-steps from its AdaLN output (already in a2) to the
-// final gated residual.  next_shift/next_scale: the following block's AdaLN-1
-// vectors to emit into a2 from the residual kernel, or NULL.
-h3dit_status run_block_body(const h3dit_config* c, const h3dit_block_weights* w, const float* mod, bf16* x,
-                            int n, const float* rope, const BlockBufs& B, int vt_ld,
-                            const float* next_shift, const float* next_scale, cudaStream_t s) {
-  const int d = c->d, F = c->ffn, H = c->heads, dh = c->head_dim;
-  uint8_t* a1 = B.base + B.ar.a1;
-  bf16* a2 = reinterpret_cast<bf16*>(B.base + B.ar.a2);
-  bf16* a3 = reinterpret_cast<bf16*>(B.base + B.ar.a3);
-  bf16* q = reinterpret_cast<bf16*>(a1);
-  bf16* k = reinterpret_cast<bf16*>(a1 + round_up((size_t)n * d * 2, 256));
-  bf16* vt = reinterpret_cast<bf16*>(a1 + 2 * round_up((size_t)n * d * 2, 256));
-  bf16* u = reinterpret_cast<bf16*>(a1);
-  const float* gate1 = mod + 2 * d;
-  const float* shift2 = mod + 3 * d;
-  const float* scale2 = mod + 4 * d;
-  const float* gate2 = mod + 5 * d;
-  if (c->precision == H3DIT_INT8)
-    return run_block_body_i8(c, w, mod, x, n, rope, B, vt_ld, next_shift, next_scale, s);
-
-  h3::GemmArgs g{};
-  g.q = q; g.k = k; g.vt = vt; g.vt_ld = vt_ld; g.d = d; g.head_dim = dh;
-  g.rope = reinterpret_cast<const float2*>(rope);
-  H3_TRY(launch_gemm(h3::kEpiQKV, a2, w->w_qkv, n, 3 * d, d, g, kQKV, s));
-  H3_TRY(launch_attention(c, q, k, vt, vt_ld, n, a2, s));
-  h3::GemmArgs go{};
-  go.c = a3; go.ldc = d;
-  H3_TRY(launch_gemm(h3::kEpiStore, a2, w->w_o, n, d, d, go, kOProj, s));
-  H3_TRY(launch_rows(x, a3, gate1, shift2, scale2, a2, nullptr, n, d, c->eps, s));
-  h3::GemmArgs g1{};
-  g1.c = u; g1.ldc = F;
-  H3_TRY(launch_gemm(h3::kEpiGelu, a2, w->w1, n, F, d, g1, kFC1, s));
-  h3::GemmArgs g2{};
-  g2.c = a3; g2.ldc = d;
-  H3_TRY(launch_gemm(h3::kEpiStore, u, w->w2, n, d, F, g2, kFC2, s));
-  H3_TRY(launch_rows(x, a3, gate2, next_shift, next_scale, a2, nullptr, n, d, c->eps, s));
-  (void)H;
+  if (q8.fc2) {
+    H3_TRY(launch_quantize_codes(u, n, F, g2, u, sc_grp, s));
+    H3_TRY(launch_gemm_i8(h3::kEpiStore, u, sc_grp, g2, w->w2, w->s2, n, d, F, gm, nullptr, kFC2, s));
+  } else {
+    H3_TRY(launch_gemm(h3::kEpiStore, u, w->w2, n, d, F, gm, kFC2, s));
+  }
+  H3_TRY(launch_rows(x, a3, gate2, next_shift, next_scale, a2, (next_shift && q8.qkv) ? sc_row : nullptr, n, d,
+                     c->eps, s));
   return H3DIT_OK;
 }
 
 h3dit_status check_weights(const h3dit_config* c, const h3dit_block_weights* w) {
   if (!w) return fail(H3DIT_E_INVAL, "weights are NULL");
   if (!w->w_qkv || !w->w_o || !w->w1 || !w->w2) return fail(H3DIT_E_INVAL, "a weight pointer is NULL");
-  if (c->precision == H3DIT_INT8) {
-    if (!w->s_qkv || !w->s_o || !w->s1 || !w->s2) return fail(H3DIT_E_INVAL, "int8 weights need scales");
-  }
+  const Int8Set q8 = int8_set(c->precision);
+  if ((q8.qkv && !w->s_qkv) || (q8.o && !w->s_o) || (q8.fc1 && !w->s1) || (q8.fc2 && !w->s2))
+    return fail(H3DIT_E_INVAL, "an int8 projection needs its weight scales");
   return H3DIT_OK;
 }
 
@@ -735,7 +732,7 @@ h3dit_status h3dit_block_forward(const h3dit_config* cfg, const h3dit_block_weig
   bf16* xb = static_cast<bf16*>(x);
   const int d = cfg->d;
   H3_TRY(launch_rope_table(cfg, pos, n_tokens, rope, stream));
-  float* hs = cfg->precision == H3DIT_INT8 ? reinterpret_cast<float*>(B.base + ar.sc_row) : nullptr;
+  float* hs = int8_set(cfg->precision).qkv ? reinterpret_cast<float*>(B.base + ar.sc_row) : nullptr;
   H3_TRY(launch_rows(xb, nullptr, nullptr, mod + 0 * d, mod + 1 * d, B.base + ar.a2, hs, n_tokens, d, cfg->eps,
                      stream));
   return run_block_body(cfg, w, mod, xb, n_tokens, rope, B, ar.vt_ld, nullptr, nullptr, stream);
@@ -786,7 +783,7 @@ h3dit_status h3dit_step_forward(const h3dit_config* cfg, const h3dit_block_weigh
   int cur_n = n_tokens;
   const float* cur_rope = rope_full;
   bool reduced = false;
-  float* hs = cfg->precision == H3DIT_INT8 ? reinterpret_cast<float*>(B.base + ar.sc_row) : nullptr;
+  float* hs = int8_set(cfg->precision).qkv ? reinterpret_cast<float*>(B.base + ar.sc_row) : nullptr;
   H3_TRY(launch_rows(cur, nullptr, nullptr, mods, mods + d, B.base + ar.a2, hs, cur_n, d, cfg->eps, stream));
   for (int b = 0; b < n_blocks; ++b) {
     const float* mod = mods + (size_t)6 * d * b;

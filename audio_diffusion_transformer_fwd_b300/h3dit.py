@@ -19,7 +19,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libh3dit.so")
 
 OK, E_INVAL, E_UNSUPPORTED, E_NOMEM, E_CUDA, E_TIMEOUT = range(6)
-BF16, INT8 = 0, 1
+BF16, INT8, INT8_MLP, INT8_QKV = 0, 1, 2, 3
 # kernel classes of h3dit_timing_read
 KC_ROWS, KC_QKV, KC_ATTN, KC_OPROJ, KC_FC1, KC_FC2, KC_REDUCE, KC_QUANT = range(8)
 

@@ -416,12 +416,12 @@ def run_ours(args):
 
 
 def run_int8_block(args, H, synth, torch, stream, barrier, max_over_ranks, rank, wdev, mod, x, pos):
-    """The 512-class block on the dynamic-int8 path: the BF16 weights
-    quantised per output channel by the library, widened to operand form
-    once (outside the timed region), then timed like the BF16 block."""
+    """The 512-class block on the dynamic-int8 paths: all four projections in
+    int8 (config 3), the MLP alone and QKV alone.  The BF16 weights are
+    quantised per output channel by the library and widened to operand form
+    once, outside the timed region; each variant is timed like the BF16 block."""
     w = synth.WORKLOADS["block_512_int8"]
     n, d, f = w.n_tokens, w.d, w.ffn
-    shape = H.BlockShape(w.d, w.heads, w.head_dim, w.ffn, w.eps, w.sections, w.theta, H.INT8)
     codes, scales = {}, {}
     for k, t in wdev.items():
         q8 = torch.empty(t.shape, device="cuda", dtype=torch.int8)
@@ -431,49 +431,54 @@ def run_int8_block(args, H, synth, torch, stream, barrier, max_over_ranks, rank,
         H.h3dit_widen_codes(q8, q8.numel(), cb, stream)
         codes[k], scales[k] = cb, sc
         del q8
-    bw = H.block_weights(codes["w_qkv"], codes["w_o"], codes["w1"], codes["w2"],
-                         scales["w_qkv"], scales["w_o"], scales["w1"], scales["w2"])
-    nbytes = H.h3dit_workspace_size(shape, n)
-    wsb = torch.empty(nbytes, device="cuda", dtype=torch.uint8)
-    x8 = x.clone()
-
-    def step():
-        H.h3dit_block_forward(shape, bw, mod, x8, pos, n, wsb, nbytes, stream)
-
-    for _ in range(args.warmup):
-        step()
-    H.h3dit_check_device_error(stream)
-    steps = max(1, min(args.steps, 100))
-    H.h3dit_timing_reset()
-    H.h3dit_timing_enable(True)
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        step()
-    e1.record(stream)
-    barrier()
-    H.h3dit_timing_enable(False)
-    H.h3dit_check_device_error(stream)
-    ms = max_over_ranks(e0.elapsed_time(e1)) / steps
-    cls = {name: H.h3dit_timing_read(k) for name, k in
-           (("qkv", H.KC_QKV), ("out_proj", H.KC_OPROJ), ("fc1", H.KC_FC1), ("fc2", H.KC_FC2),
-            ("attention", H.KC_ATTN), ("rows", H.KC_ROWS), ("quant", H.KC_QUANT))}
-    gemm_ms = sum(cls[k][0] for k in ("qkv", "out_proj", "fc1", "fc2")) / steps
-    gops = gemm_flops(n, d, f)
+    names = ("w_qkv", "w_o", "w1", "w2")
+    variants = (("int8", H.INT8, names), ("int8_mlp", H.INT8_MLP, ("w1", "w2")), ("int8_qkv", H.INT8_QKV, ("w_qkv",)))
     burst, _, _, peak_src = measured_peaks()
-    res = {
-        "workload": "block_512_int8: the block_512 shapes with int8 QKV/out-proj/FC1/FC2 (per-token activation "
-                    "scales, per-output-channel weight scales, FC2 one scale per 1024 input channels), BF16 attention",
-        "ms": ms, "tops": block_flops(n, d, f) / (ms * 1e-3) / 1e12,
-        "gemm_ms": gemm_ms, "gemm_tops": gops / (gemm_ms * 1e-3) / 1e12,
-        "gemm_frac_of_bf16_burst": gops / (gemm_ms * 1e-3) / 1e12 / burst,
-        "peak_note": f"int8 codes run exactly on the BF16 tensor path (sm_103a has no integer tcgen05 MMA): "
-                     f"peak = {peak_src} bf16 burst {burst}",
-        "quant_ms": cls["quant"][0] / steps, "rows_ms": cls["rows"][0] / steps,
-        "attention_ms": cls["attention"][0] / steps, "steps": steps,
-    }
-    del wsb, codes
+    gops = gemm_flops(n, d, f)
+    res = {"workload": "block_512_int8: the block_512 shapes with int8 QKV/out-proj/FC1/FC2 (per-token activation "
+                       "scales, per-output-channel weight scales, FC2 one scale per 1024 input channels), BF16 attention; "
+                       "variants with the MLP alone and QKV alone in int8",
+           "peak_note": f"int8 codes run exactly on the BF16 tensor path (sm_103a has no integer tcgen05 MMA): "
+                        f"peak = {peak_src} bf16 burst {burst}"}
+    for name, prec, q_names in variants:
+        shape = H.BlockShape(w.d, w.heads, w.head_dim, w.ffn, w.eps, w.sections, w.theta, prec)
+        ptr = [codes[k] if k in q_names else wdev[k] for k in names]
+        sc = [scales[k] if k in q_names else None for k in names]
+        bw = H.block_weights(*ptr, *sc)
+        nbytes = H.h3dit_workspace_size(shape, n)
+        wsb = torch.empty(nbytes, device="cuda", dtype=torch.uint8)
+        x8 = x.clone()
+
+        def step():
+            H.h3dit_block_forward(shape, bw, mod, x8, pos, n, wsb, nbytes, stream)
+
+        for _ in range(args.warmup):
+            step()
+        H.h3dit_check_device_error(stream)
+        steps = max(1, min(args.steps, 100 if name == "int8" else 30))
+        H.h3dit_timing_reset()
+        H.h3dit_timing_enable(True)
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        barrier()
+        H.h3dit_timing_enable(False)
+        H.h3dit_check_device_error(stream)
+        ms = max_over_ranks(e0.elapsed_time(e1)) / steps
+        cls = {c: H.h3dit_timing_read(k) for c, k in
+               (("qkv", H.KC_QKV), ("out_proj", H.KC_OPROJ), ("fc1", H.KC_FC1), ("fc2", H.KC_FC2),
+                ("attention", H.KC_ATTN), ("rows", H.KC_ROWS), ("quant", H.KC_QUANT))}
+        gemm_ms = sum(cls[k][0] for k in ("qkv", "out_proj", "fc1", "fc2")) / steps
+        res[name] = {"ms": ms, "tops": block_flops(n, d, f) / (ms * 1e-3) / 1e12,
+                     "gemm_ms": gemm_ms, "gemm_tops": gops / (gemm_ms * 1e-3) / 1e12,
+                     "gemm_frac_of_bf16_burst": gops / (gemm_ms * 1e-3) / 1e12 / burst,
+                     "quant_ms": cls["quant"][0] / steps, "rows_ms": cls["rows"][0] / steps,
+                     "attention_ms": cls["attention"][0] / steps, "steps": steps}
+        del wsb
+    del codes
     torch.cuda.empty_cache()
     return res
 

@@ -56,7 +56,11 @@ typedef enum {
   H3DIT_E_TIMEOUT = 5       /* a kernel's bounded pipeline wait ran out */
 } h3dit_status;
 
-typedef enum { H3DIT_BF16 = 0, H3DIT_INT8 = 1 } h3dit_precision;
+/* Which projections run on dynamic int8 ([linlog] "int8 量化：从 36 秒到 19 秒"
+ * compares the MLP alone, QKV alone and all four): H3DIT_INT8 = QKV,
+ * out-projection, FC1 and FC2; H3DIT_INT8_MLP = FC1 and FC2; H3DIT_INT8_QKV =
+ * the QKV projection only.  The other projections run in BF16. */
+typedef enum { H3DIT_BF16 = 0, H3DIT_INT8 = 1, H3DIT_INT8_MLP = 2, H3DIT_INT8_QKV = 3 } h3dit_precision;
 
 /* Shape of one block.  The pages give none of these numbers.
  *  d            model width; a multiple of 256, at most 8192
@@ -66,7 +70,7 @@ typedef enum { H3DIT_BF16 = 0, H3DIT_INT8 = 1 } h3dit_precision;
  *  eps          LayerNorm epsilon (LayerNorm: biased variance, no affine)
  *  rope_sections head-dim widths of the (t, y, x) RoPE sections; even, sum head_dim
  *  rope_theta   RoPE base; pair i of a section of width s turns by pos * theta^(-2i/s)
- *  precision    H3DIT_BF16 or H3DIT_INT8 (dynamic-int8 projections) */
+ *  precision    an h3dit_precision: which projections are dynamic int8 */
 typedef struct {
   int d;
   int heads;
@@ -78,9 +82,12 @@ typedef struct {
   int precision;
 } h3dit_config;
 
-/* One block's projection weights, device pointers.
- * BF16 precision: BF16 [out][in] matrices, scale pointers unused (may be NULL).
- * INT8 precision: per-output-channel int8 codes [out][in] in operand form --
+/* One block's projection weights, device pointers.  Each projection is BF16
+ * or int8 as the config's precision says (the other form of that projection
+ * is never read):
+ * BF16 projection: a BF16 [out][in] matrix; its scale pointer is unused (may
+ *   be NULL).
+ * int8 projection: per-output-channel int8 codes [out][in] in operand form --
  *   each code stored as the BF16 value of the same integer (exact), the form
  *   the tensor cores read, made once from int8 codes by h3dit_widen_codes --
  *   and fp32 per-output-channel scales (h3dit_quantize_weight), as in [linlog]
@@ -168,12 +175,12 @@ h3dit_status h3dit_workspace_size(const h3dit_config* cfg, int n_tokens,
  * x:   device BF16 [n_tokens][d], read and overwritten.
  * pos: device fp32 [n_tokens][3] (t, y, x) rotary positions.
  * ws:  device workspace of at least h3dit_workspace_size bytes, 256-byte aligned.
- * With precision H3DIT_INT8 the four projections run on int8 codes
- * ([linlog] "int8 量化"): h, o and h2 are quantised per token, u per token and
- * per 1024 channels (h3dit_quantize_act's rule on their BF16 values), the
- * weights are operand-form codes with per-output-channel scales, and the
- * outputs are dequantised to BF16 as h3dit_linear_i8 states; attention stays
- * BF16.  INT8 needs ffn <= 1024 or ffn % 1024 == 0.
+ * With an int8 precision the selected projections run on int8 codes
+ * ([linlog] "int8 量化"): their inputs (h, o, h2 per token; u per token and
+ * per 1024 channels) are quantised with h3dit_quantize_act's rule on the BF16
+ * values, the weights are operand-form codes with per-output-channel scales,
+ * and the outputs are dequantised to BF16 as h3dit_linear_i8 states;
+ * attention stays BF16.  An int8 FC2 needs ffn <= 1024 or ffn % 1024 == 0.
  * Errors: E_INVAL (nulls, n_tokens < 1), E_UNSUPPORTED (shape outside the
  * limits of h3dit_config), E_NOMEM (ws_bytes too small), E_CUDA. */
 h3dit_status h3dit_block_forward(const h3dit_config* cfg, const h3dit_block_weights* w,

@@ -58,7 +58,7 @@ __all__ = [
     "BlockConfig", "VideoGrid", "Reduction",
     "bf16_round", "layer_norm", "adaln", "rope_angles", "apply_rope",
     "attention", "gelu_tanh", "block_forward", "step_forward",
-    "quantize_rows", "quantize_weight", "gemm_int", "linear_int8",
+    "quantize_rows", "quantize_weight", "gemm_int", "linear_int8", "INT8_ALL", "INT8_MLP", "INT8_QKV",
     "fc2_int8", "block_forward_int8",
     "reduced_token_count", "token_reduce", "token_restore",
     "reduced_positions", "block_flops",
@@ -456,17 +456,26 @@ def fc2_int8(uq, us, wq, ws, group: int = 1024) -> np.ndarray:
     return out * np.asarray(ws, np.float64).reshape(1, -1)
 
 
+INT8_ALL = ("qkv", "o", "fc1", "fc2")
+INT8_MLP = ("fc1", "fc2")
+INT8_QKV = ("qkv",)
+
+
 def block_forward_int8(x, w: Dict[str, np.ndarray], mod, pos, cfg: BlockConfig,
                        bf16_storage: bool = True, fc2_group: int = 1024, return_parts: bool = False,
-                       rows=None):
+                       rows=None, which=INT8_ALL):
     """The block of ``block_forward`` on the dynamic-int8 path.
 
-    w holds int8 codes ``q_qkv, q_o, q1, q2`` and fp32 per-output-channel
-    scales ``s_qkv, s_o, s1, s2``.  QKV, out-projection and FC1 quantise their
-    input per token; FC2 quantises per token and per ``fc2_group`` input
-    channels.  Attention itself stays in floating point.  ``rows`` evaluates
-    the output only for those query rows (every quantisation after QKV is per
-    token, so the rows are independent once keys and values exist)."""
+    ``which`` names the projections that run in int8 ([linlog] "int8 量化":
+    the MLP alone, QKV alone, or all four); the others use the BF16 weights
+    ``w_qkv, w_o, w1, w2`` exactly as ``block_forward``.  For an int8
+    projection w holds int8 codes (``q_qkv, q_o, q1, q2``) and fp32
+    per-output-channel scales (``s_qkv, s_o, s1, s2``).  QKV, out-projection
+    and FC1 quantise their input per token; FC2 quantises per token and per
+    ``fc2_group`` input channels.  Attention itself stays in floating point.
+    ``rows`` evaluates the output only for those query rows (every
+    quantisation after QKV is per token, so the rows are independent once keys
+    and values exist)."""
     R = lambda a: _maybe_round(a, bf16_storage)
     x = np.asarray(x, dtype=np.float64)
     mod = np.asarray(mod, dtype=np.float64)
@@ -475,21 +484,37 @@ def block_forward_int8(x, w: Dict[str, np.ndarray], mod, pos, cfg: BlockConfig,
     f = cfg.ffn
     g2 = min(fc2_group, f)
     h = R(adaln(x, shift1, scale1, cfg.eps))
-    hq, hs = quantize_rows(h)
-    qkv = linear_int8(hq, hs, w["q_qkv"], w["s_qkv"])
+    if "qkv" in which:
+        hq, hs = quantize_rows(h)
+        qkv = linear_int8(hq, hs, w["q_qkv"], w["s_qkv"])
+    else:
+        hq = hs = None
+        qkv = h @ np.asarray(w["w_qkv"], np.float64).T
     q = R(apply_rope(_split_heads(qkv[:, 0:d], cfg).transpose(1, 0, 2), pos, cfg)).transpose(1, 0, 2)
     k = R(apply_rope(_split_heads(qkv[:, d:2 * d], cfg).transpose(1, 0, 2), pos, cfg)).transpose(1, 0, 2)
     v = R(_split_heads(qkv[:, 2 * d:3 * d], cfg))
     sel = slice(None) if rows is None else np.asarray(rows)
     o = R(_merge_heads(attention(q, k, v, rows=rows)))
-    oq, os_ = quantize_rows(o)
-    a = R(linear_int8(oq, os_, w["q_o"], w["s_o"]))
+    if "o" in which:
+        oq, os_ = quantize_rows(o)
+        a = R(linear_int8(oq, os_, w["q_o"], w["s_o"]))
+    else:
+        oq = os_ = None
+        a = R(o @ np.asarray(w["w_o"], np.float64).T)
     x1 = R(x[sel] + gate1 * a)
     h2 = R(adaln(x1, shift2, scale2, cfg.eps))
-    h2q, h2s = quantize_rows(h2)
-    u = R(gelu_tanh(linear_int8(h2q, h2s, w["q1"], w["s1"])))
-    uq, us = quantize_rows(u, g2)
-    m = R(fc2_int8(uq, us, w["q2"], w["s2"], g2))
+    if "fc1" in which:
+        h2q, h2s = quantize_rows(h2)
+        u = R(gelu_tanh(linear_int8(h2q, h2s, w["q1"], w["s1"])))
+    else:
+        h2q = h2s = None
+        u = R(gelu_tanh(h2 @ np.asarray(w["w1"], np.float64).T))
+    if "fc2" in which:
+        uq, us = quantize_rows(u, g2)
+        m = R(fc2_int8(uq, us, w["q2"], w["s2"], g2))
+    else:
+        uq = us = None
+        m = R(u @ np.asarray(w["w2"], np.float64).T)
     x2 = R(x1 + gate2 * m)
     if return_parts:
         return x2, dict(h=h, hq=hq, hs=hs, qkv=qkv, q=q, k=k, v=v, o=o, oq=oq, os=os_, a=a,

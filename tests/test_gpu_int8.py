@@ -302,3 +302,76 @@ def test_int8_step_of_one_block_equals_block_and_chains():
     got = host(xs)
     assert rel_l2(got, ref_bf) <= 1e-2 * nb
     assert rel_l2(got - x, ref_bf - x) <= 2e-2 * nb
+
+
+def _mixed_weights(wt, which):
+    """Device weights for a block whose projections in ``which`` are int8
+    (operand-form codes + scales) and the rest BF16; host dict with both
+    forms for the oracle."""
+    names = {"qkv": ("w_qkv", "q_qkv", "s_qkv"), "o": ("w_o", "q_o", "s_o"), "fc1": ("w1", "q1", "s1"),
+             "fc2": ("w2", "q2", "s2")}
+    hw = dict(wt)
+    ptrs, scales, keep = [], [], []
+    for key in ("qkv", "o", "fc1", "fc2"):
+        wn, qn, sn = names[key]
+        q, s = O.quantize_weight(wt[wn])
+        hw[qn], hw[sn] = q, s[:, 0]
+        if key in which:
+            dw, ds = codes_dev(q), dev_f32(s[:, 0])
+        else:
+            dw, ds = dev_bf16(wt[wn]), None
+        keep += [dw, ds]
+        ptrs.append(dw)
+        scales.append(ds)
+    bw = H.block_weights(*ptrs, *scales)
+    return hw, bw, keep
+
+
+@pytest.mark.parametrize("prec,which", [(H.INT8_MLP, O.INT8_MLP), (H.INT8_QKV, O.INT8_QKV)])
+def test_int8_variant_block_tiny(prec, which):
+    """The MLP-only and QKV-only int8 blocks against the oracle's block with
+    the same projections in int8."""
+    w = TINY
+    n = w.n_tokens
+    pos = synth.positions(w.video, w.n_text, w.n_audio)
+    x = synth.host_activations(n, w.d, seed=21)
+    wt = synth.host_block_weights(w.d, w.ffn, seed=21)
+    mod = synth.host_mod(w.d, seed=21)
+    hw, bw, keep = _mixed_weights(wt, which)
+    shape = shape_of(w, prec)
+    xd = dev_bf16(x)
+    nbytes = H.h3dit_workspace_size(shape, n)
+    ws = torch.empty(nbytes, device="cuda", dtype=torch.uint8)
+    H.h3dit_block_forward(shape, bw, dev_f32(mod), xd, dev_f32(pos), n, ws, nbytes)
+    H.h3dit_check_device_error()
+    got = host(xd)
+    cfg = oracle_cfg(w)
+    ref_bf = O.block_forward_int8(x, hw, mod, pos, cfg, bf16_storage=True, which=which)
+    ref64 = O.block_forward_int8(x, hw, mod, pos, cfg, bf16_storage=False, which=which)
+    assert_block(got, x, ref64, ref_bf)
+    # and it is not the full-int8 or the BF16 block
+    full = O.block_forward_int8(x, hw, mod, pos, cfg, bf16_storage=True)
+    bf = O.block_forward(x, wt, mod, pos, cfg, bf16_storage=True)
+    assert rel_l2(got - x, ref_bf - x) < min(rel_l2(got - x, full - x), rel_l2(got - x, bf - x))
+
+
+@pytest.mark.parametrize("prec", [H.INT8_MLP, H.INT8_QKV])
+def test_int8_variant_step_equals_blocks(prec):
+    which = O.INT8_MLP if prec == H.INT8_MLP else O.INT8_QKV
+    w = TINY
+    n = w.n_tokens
+    shape = shape_of(w, prec)
+    pos = synth.positions(w.video, w.n_text, w.n_audio)
+    x = synth.host_activations(n, w.d, seed=22)
+    nb = 3
+    packs = [_mixed_weights(synth.host_block_weights(w.d, w.ffn, seed=22, block=b), which) for b in range(nb)]
+    mods = np.stack([synth.host_mod(w.d, seed=22, block=b) for b in range(nb)])
+    nbytes = H.h3dit_workspace_size(shape, n)
+    ws = torch.empty(nbytes, device="cuda", dtype=torch.uint8)
+    xs = dev_bf16(x)
+    H.h3dit_step_forward(shape, [p[1] for p in packs], dev_f32(mods), xs, dev_f32(pos), n, None, ws, nbytes)
+    xb = dev_bf16(x)
+    for b in range(nb):
+        H.h3dit_block_forward(shape, packs[b][1], dev_f32(mods[b]), xb, dev_f32(pos), n, ws, nbytes)
+    H.h3dit_check_device_error()
+    assert torch.equal(xs, xb)

@@ -475,3 +475,31 @@ def test_int8_block_rows_match_full_evaluation():
     part = O.block_forward_int8(x, wq, mod, pos, cfg, bf16_storage=False, fc2_group=64, rows=rows)
     assert np.allclose(part, full[rows], rtol=0, atol=1e-12)
 
+
+def test_int8_block_without_int8_projections_is_the_float_block():
+    """With no projection in int8 the mixed-precision block is the BF16 block
+    (same storage points), bit for bit; MLP-only and QKV-only sit between."""
+    cfg = O.BlockConfig(d=64, heads=2, head_dim=32, ffn=128, rope_sections=(8, 12, 12))
+    r = np.random.default_rng(17)
+    n = 20
+    w = {"w_qkv": r.standard_normal((192, 64)) * 0.1, "w_o": r.standard_normal((64, 64)) * 0.1,
+         "w1": r.standard_normal((128, 64)) * 0.1, "w2": r.standard_normal((64, 128)) * 0.1}
+    for name, qn, sn in (("w_qkv", "q_qkv", "s_qkv"), ("w_o", "q_o", "s_o"), ("w1", "q1", "s1"), ("w2", "q2", "s2")):
+        w[qn], sc = O.quantize_weight(w[name])
+        w[sn] = sc[:, 0]
+    mod = r.standard_normal((6, 64)) * 0.3
+    x = r.standard_normal((n, 64))
+    pos = r.uniform(0, 5, (n, 3))
+    for storage in (False, True):
+        ref = O.block_forward(x, w, mod, pos, cfg, bf16_storage=storage)
+        none = O.block_forward_int8(x, w, mod, pos, cfg, bf16_storage=storage, fc2_group=64, which=())
+        assert np.array_equal(none, ref)
+    ref = O.block_forward(x, w, mod, pos, cfg)
+    errs = {}
+    for which in (O.INT8_QKV, O.INT8_MLP, O.INT8_ALL):
+        got = O.block_forward_int8(x, w, mod, pos, cfg, bf16_storage=False, fc2_group=64, which=which)
+        errs[which] = np.linalg.norm((got - x) - (ref - x)) / np.linalg.norm(ref - x)
+        assert 0 < errs[which] < 3e-2
+    # quantising more projections adds error
+    assert errs[O.INT8_ALL] > max(errs[O.INT8_QKV], errs[O.INT8_MLP])
+
