@@ -385,11 +385,12 @@ bool fusion_disabled() {
 
 template <bool GATE, bool NORM, bool QUANT>
 void launch_row_kernel(int nv, bf16* x, const bf16* branch, const float* gate, const float* shift,
-                       const float* scale, bf16* h, float* hs, int n, int d, float eps, cudaStream_t s) {
+                       const float* scale, bf16* h, float* hs, int n, int d, float eps, const h3::SegMap& sm,
+                       cudaStream_t s) {
 #define H3_ROW_CASE(NVV)                                                                               \
   case NVV:                                                                                            \
     h3::gate_adaln_kernel<GATE, NORM, QUANT, NVV><<<n, h3::kRowThreads, 0, s>>>(x, branch, gate, shift, \
-                                                                                 scale, h, hs, d, eps); \
+                                                                                 scale, h, hs, d, eps, sm); \
     break;
   switch (nv) {
     H3_ROW_CASE(1) H3_ROW_CASE(2) H3_ROW_CASE(3) H3_ROW_CASE(4)
@@ -401,8 +402,15 @@ void launch_row_kernel(int nv, bf16* x, const bf16* branch, const float* gate, c
 // Gated residual (branch != NULL) and/or AdaLN (shift != NULL).  hs != NULL
 // selects the int8 form of the AdaLN output: h receives the row's int8 codes
 // as BF16 values and hs[row] the scale.
+h3::SegMap one_segment() {
+  h3::SegMap m{};
+  m.count = 1;
+  return m;
+}
+
 h3dit_status launch_rows(void* x, const void* branch, const float* gate, const float* shift, const float* scale,
-                         void* h, float* hs, int n, int d, float eps, cudaStream_t s) {
+                         void* h, float* hs, int n, int d, float eps, cudaStream_t s,
+                         const h3::SegMap& sm = one_segment()) {
   TimedLaunch tl(kRows, s);
   bf16* xb = static_cast<bf16*>(x);
   const bf16* bb = static_cast<const bf16*>(branch);
@@ -415,17 +423,17 @@ h3dit_status launch_rows(void* x, const void* branch, const float* gate, const f
   const int nv = (d / 8 + h3::kRowThreads - 1) / h3::kRowThreads;
   if (gate_on && norm_on && !fusion_disabled()) {
     if (quant)
-      launch_row_kernel<true, true, true>(nv, xb, bb, gate, shift, scale, hb, hs, n, d, eps, s);
+      launch_row_kernel<true, true, true>(nv, xb, bb, gate, shift, scale, hb, hs, n, d, eps, sm, s);
     else
-      launch_row_kernel<true, true, false>(nv, xb, bb, gate, shift, scale, hb, nullptr, n, d, eps, s);
+      launch_row_kernel<true, true, false>(nv, xb, bb, gate, shift, scale, hb, nullptr, n, d, eps, sm, s);
   } else {
     if (gate_on)
-      launch_row_kernel<true, false, false>(nv, xb, bb, gate, nullptr, nullptr, nullptr, nullptr, n, d, eps, s);
+      launch_row_kernel<true, false, false>(nv, xb, bb, gate, nullptr, nullptr, nullptr, nullptr, n, d, eps, sm, s);
     if (norm_on) {
       if (quant)
-        launch_row_kernel<false, true, true>(nv, xb, nullptr, nullptr, shift, scale, hb, hs, n, d, eps, s);
+        launch_row_kernel<false, true, true>(nv, xb, nullptr, nullptr, shift, scale, hb, hs, n, d, eps, sm, s);
       else
-        launch_row_kernel<false, true, false>(nv, xb, nullptr, nullptr, shift, scale, hb, nullptr, n, d, eps, s);
+        launch_row_kernel<false, true, false>(nv, xb, nullptr, nullptr, shift, scale, hb, nullptr, n, d, eps, sm, s);
     }
   }
   H3_CUDA(cudaGetLastError());
@@ -519,7 +527,8 @@ struct BlockBufs {
 // kernel (as codes if that block's QKV is int8), or NULL.
 h3dit_status run_block_body(const h3dit_config* c, const h3dit_block_weights* w, const float* mod, bf16* x,
                             int n, const float* rope, const BlockBufs& B, int vt_ld,
-                            const float* next_shift, const float* next_scale, cudaStream_t s) {
+                            const float* next_shift, const float* next_scale, cudaStream_t s,
+                            const h3::SegMap& sm) {
   const int d = c->d, F = c->ffn, dh = c->head_dim;
   const Int8Set q8 = int8_set(c->precision);
   const int g2 = fc2_group(c);
@@ -555,7 +564,7 @@ h3dit_status run_block_body(const h3dit_config* c, const h3dit_block_weights* w,
     H3_TRY(launch_attention(c, q, k, vt, vt_ld, n, a2, s));
     H3_TRY(launch_gemm(h3::kEpiStore, a2, w->w_o, n, d, d, go, kOProj, s));
   }
-  H3_TRY(launch_rows(x, a3, gate1, shift2, scale2, a2, q8.fc1 ? sc_row : nullptr, n, d, c->eps, s));
+  H3_TRY(launch_rows(x, a3, gate1, shift2, scale2, a2, q8.fc1 ? sc_row : nullptr, n, d, c->eps, s, sm));
   h3::GemmArgs g1{};
   g1.c = u; g1.ldc = F;
   if (q8.fc1)
@@ -571,7 +580,41 @@ h3dit_status run_block_body(const h3dit_config* c, const h3dit_block_weights* w,
     H3_TRY(launch_gemm(h3::kEpiStore, u, w->w2, n, d, F, gm, kFC2, s));
   }
   H3_TRY(launch_rows(x, a3, gate2, next_shift, next_scale, a2, (next_shift && q8.qkv) ? sc_row : nullptr, n, d,
-                     c->eps, s));
+                     c->eps, s, sm));
+  return H3DIT_OK;
+}
+
+// The segment map of a modulation table [count][6][d]; NULL segments = one.
+h3dit_status make_segmap(const h3dit_segments* seg, int n_tokens, int d, h3::SegMap* out) {
+  h3::SegMap m{};
+  m.count = 1;
+  m.stride = 6 * d;
+  if (seg) {
+    if (seg->count < 1 || seg->count > 4) return fail(H3DIT_E_INVAL, "segment count %d (1..4)", seg->count);
+    if (seg->start[0] != 0) return fail(H3DIT_E_INVAL, "the first segment must start at row 0");
+    for (int i = 1; i < seg->count; ++i)
+      if (seg->start[i] <= seg->start[i - 1] || seg->start[i] >= n_tokens)
+        return fail(H3DIT_E_INVAL, "segment starts must increase and lie inside the %d rows", n_tokens);
+    m.count = seg->count;
+    for (int i = 0; i < seg->count; ++i) m.start[i] = seg->start[i];
+  }
+  *out = m;
+  return H3DIT_OK;
+}
+
+// The segment map of the reduced stream: boundaries before the video grid
+// stay, boundaries after it move up by the rows the pairing removed; a
+// boundary inside the grid is refused (a pair must lie in one segment).
+h3dit_status reduce_segmap(const h3::SegMap& m, const h3::PairGrid& g, h3::SegMap* out) {
+  h3::SegMap r = m;
+  const int v0 = g.offset, v1 = g.offset + g.T * g.Hh * g.W;
+  const int removed = g.n_full - g.n_red;
+  for (int i = 1; i < m.count; ++i) {
+    if (m.start[i] <= v0) continue;
+    if (m.start[i] < v1) return fail(H3DIT_E_INVAL, "segment start %d lies inside the reduced video grid", m.start[i]);
+    r.start[i] = m.start[i] - removed;
+  }
+  *out = r;
   return H3DIT_OK;
 }
 
@@ -717,14 +760,16 @@ h3dit_status h3dit_linear(const void* a, const void* b, int m, int n, int k, int
   return launch_gemm(act ? h3::kEpiGelu : h3::kEpiStore, a, b, m, n, k, g, act ? kFC1 : kOProj, stream);
 }
 
-h3dit_status h3dit_block_forward(const h3dit_config* cfg, const h3dit_block_weights* w, const float* mod,
-                                 void* x, const float* pos, int n_tokens, void* ws, size_t ws_bytes,
-                                 cudaStream_t stream) {
+static h3dit_status block_forward_impl(const h3dit_config* cfg, const h3dit_block_weights* w, const float* mod,
+                                const h3dit_segments* seg, void* x, const float* pos, int n_tokens, void* ws,
+                                size_t ws_bytes, cudaStream_t stream) {
   H3_TRY(check_cfg(cfg));
   H3_TRY(check_weights(cfg, w));
   if (!mod || !x || !pos || !ws) return fail(H3DIT_E_INVAL, "NULL pointer");
   if (n_tokens < 1) return fail(H3DIT_E_INVAL, "n_tokens %d", n_tokens);
   if (!aligned(ws, 256) || !aligned(x, 16)) return fail(H3DIT_E_INVAL, "ws must be 256-byte and x 16-byte aligned");
+  h3::SegMap sm;
+  H3_TRY(make_segmap(seg, n_tokens, cfg->d, &sm));
   const Arena ar = plan_arena(cfg, n_tokens, nullptr);
   if (ws_bytes < ar.total) return fail(H3DIT_E_NOMEM, "workspace %zu < %zu bytes", ws_bytes, ar.total);
   BlockBufs B{static_cast<uint8_t*>(ws), ar};
@@ -734,13 +779,13 @@ h3dit_status h3dit_block_forward(const h3dit_config* cfg, const h3dit_block_weig
   H3_TRY(launch_rope_table(cfg, pos, n_tokens, rope, stream));
   float* hs = int8_set(cfg->precision).qkv ? reinterpret_cast<float*>(B.base + ar.sc_row) : nullptr;
   H3_TRY(launch_rows(xb, nullptr, nullptr, mod + 0 * d, mod + 1 * d, B.base + ar.a2, hs, n_tokens, d, cfg->eps,
-                     stream));
-  return run_block_body(cfg, w, mod, xb, n_tokens, rope, B, ar.vt_ld, nullptr, nullptr, stream);
+                     stream, sm));
+  return run_block_body(cfg, w, mod, xb, n_tokens, rope, B, ar.vt_ld, nullptr, nullptr, stream, sm);
 }
 
-h3dit_status h3dit_step_forward(const h3dit_config* cfg, const h3dit_block_weights* w, int n_blocks,
-                                const float* mods, void* x, const float* pos, int n_tokens,
-                                const h3dit_reduction* tr, void* ws, size_t ws_bytes, cudaStream_t stream) {
+static h3dit_status step_forward_impl(const h3dit_config* cfg, const h3dit_block_weights* w, int n_blocks,
+                               const float* mods, const h3dit_segments* seg, void* x, const float* pos, int n_tokens,
+                               const h3dit_reduction* tr, void* ws, size_t ws_bytes, cudaStream_t stream) {
   H3_TRY(check_cfg(cfg));
   if (!w || n_blocks < 0) return fail(H3DIT_E_INVAL, "weights NULL or n_blocks < 0");
   if (n_blocks == 0) return H3DIT_OK;
@@ -753,6 +798,11 @@ h3dit_status h3dit_step_forward(const h3dit_config* cfg, const h3dit_block_weigh
     if (tr->reduce_after_block < 0 || tr->restore_before_block <= tr->reduce_after_block)
       return fail(H3DIT_E_INVAL, "reduction blocks %d / %d", tr->reduce_after_block, tr->restore_before_block);
   }
+  h3::SegMap sm_full;
+  H3_TRY(make_segmap(seg, n_tokens, cfg->d, &sm_full));
+  h3::SegMap sm_red = sm_full;
+  if (tr) H3_TRY(reduce_segmap(sm_full, pair_grid(&tr->grid, n_tokens), &sm_red));
+  const size_t per_block = (size_t)sm_full.count * 6 * cfg->d;   // modulation floats per block
   const Arena ar = plan_arena(cfg, n_tokens, tr);
   if (ws_bytes < ar.total) return fail(H3DIT_E_NOMEM, "workspace %zu < %zu bytes", ws_bytes, ar.total);
   BlockBufs B{static_cast<uint8_t*>(ws), ar};
@@ -784,17 +834,18 @@ h3dit_status h3dit_step_forward(const h3dit_config* cfg, const h3dit_block_weigh
   const float* cur_rope = rope_full;
   bool reduced = false;
   float* hs = int8_set(cfg->precision).qkv ? reinterpret_cast<float*>(B.base + ar.sc_row) : nullptr;
-  H3_TRY(launch_rows(cur, nullptr, nullptr, mods, mods + d, B.base + ar.a2, hs, cur_n, d, cfg->eps, stream));
+  const h3::SegMap* cur_sm = &sm_full;
+  H3_TRY(launch_rows(cur, nullptr, nullptr, mods, mods + d, B.base + ar.a2, hs, cur_n, d, cfg->eps, stream, *cur_sm));
   for (int b = 0; b < n_blocks; ++b) {
-    const float* mod = mods + (size_t)6 * d * b;
+    const float* mod = mods + per_block * b;
     const bool last = b + 1 == n_blocks;
     const bool reduce_now = tr && !reduced && b == tr->reduce_after_block && b + 1 < tr->restore_before_block && !last;
     const bool restore_now = tr && reduced && b + 1 == tr->restore_before_block && !last;
-    const float* nmod = last ? nullptr : mods + (size_t)6 * d * (b + 1);
+    const float* nmod = last ? nullptr : mods + per_block * (b + 1);
     const bool emit_next = !last && !reduce_now && !restore_now;
     const int vt_ld = (int)round_up((size_t)cur_n, 64);
     H3_TRY(run_block_body(cfg, &w[b], mod, cur, cur_n, cur_rope, B, vt_ld,
-                          emit_next ? nmod : nullptr, emit_next ? nmod + d : nullptr, stream));
+                          emit_next ? nmod : nullptr, emit_next ? nmod + d : nullptr, stream, *cur_sm));
     if (reduce_now) {
       {
         TimedLaunch tl(kReduce, stream);
@@ -805,7 +856,9 @@ h3dit_status h3dit_step_forward(const h3dit_config* cfg, const h3dit_block_weigh
       cur_n = pg.n_red;
       cur_rope = rope_red;
       reduced = true;
-      H3_TRY(launch_rows(cur, nullptr, nullptr, nmod, nmod + d, B.base + ar.a2, hs, cur_n, d, cfg->eps, stream));
+      cur_sm = &sm_red;
+      H3_TRY(launch_rows(cur, nullptr, nullptr, nmod, nmod + d, B.base + ar.a2, hs, cur_n, d, cfg->eps, stream,
+                         *cur_sm));
     } else if (restore_now) {
       {
         TimedLaunch tl(kReduce, stream);
@@ -816,7 +869,9 @@ h3dit_status h3dit_step_forward(const h3dit_config* cfg, const h3dit_block_weigh
       cur_n = n_tokens;
       cur_rope = rope_full;
       reduced = false;
-      H3_TRY(launch_rows(cur, nullptr, nullptr, nmod, nmod + d, B.base + ar.a2, hs, cur_n, d, cfg->eps, stream));
+      cur_sm = &sm_full;
+      H3_TRY(launch_rows(cur, nullptr, nullptr, nmod, nmod + d, B.base + ar.a2, hs, cur_n, d, cfg->eps, stream,
+                         *cur_sm));
     }
   }
   if (reduced) {
@@ -825,6 +880,33 @@ h3dit_status h3dit_step_forward(const h3dit_config* cfg, const h3dit_block_weigh
     H3_CUDA(cudaGetLastError());
   }
   return H3DIT_OK;
+}
+
+h3dit_status h3dit_block_forward(const h3dit_config* cfg, const h3dit_block_weights* w, const float* mod,
+                                 void* x, const float* pos, int n_tokens, void* ws, size_t ws_bytes,
+                                 cudaStream_t stream) {
+  return block_forward_impl(cfg, w, mod, nullptr, x, pos, n_tokens, ws, ws_bytes, stream);
+}
+
+h3dit_status h3dit_block_forward_seg(const h3dit_config* cfg, const h3dit_block_weights* w, const float* mods,
+                                     const h3dit_segments* seg, void* x, const float* pos, int n_tokens, void* ws,
+                                     size_t ws_bytes, cudaStream_t stream) {
+  if (!seg) return fail(H3DIT_E_INVAL, "segments are NULL");
+  return block_forward_impl(cfg, w, mods, seg, x, pos, n_tokens, ws, ws_bytes, stream);
+}
+
+h3dit_status h3dit_step_forward(const h3dit_config* cfg, const h3dit_block_weights* w, int n_blocks,
+                                const float* mods, void* x, const float* pos, int n_tokens,
+                                const h3dit_reduction* tr, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return step_forward_impl(cfg, w, n_blocks, mods, nullptr, x, pos, n_tokens, tr, ws, ws_bytes, stream);
+}
+
+h3dit_status h3dit_step_forward_seg(const h3dit_config* cfg, const h3dit_block_weights* w, int n_blocks,
+                                    const float* mods, const h3dit_segments* seg, void* x, const float* pos,
+                                    int n_tokens, const h3dit_reduction* tr, void* ws, size_t ws_bytes,
+                                    cudaStream_t stream) {
+  if (!seg) return fail(H3DIT_E_INVAL, "segments are NULL");
+  return step_forward_impl(cfg, w, n_blocks, mods, seg, x, pos, n_tokens, tr, ws, ws_bytes, stream);
 }
 
 h3dit_status h3dit_quantize_act(const void* x_bf16, int rows, int cols, int group, int8_t* q, float* scales,

@@ -50,6 +50,23 @@ __device__ __forceinline__ int quant_code(float x, float s) {
 // int8 codes of bf16(h) at s = absmax(bf16(h)) / 127 are written into h as
 // BF16 values, and s into hs[row] -- the same codes h3dit_quantize_act gives
 // for the BF16 h.
+// Token segments with their own modulation vectors ([linlog] "音频处理": the
+// reference audio is conditioned at its own timestep): segment k covers rows
+// start[k] .. start[k+1]-1, and its vectors sit `stride` floats after the
+// previous segment's.
+struct SegMap {
+  int count;      // 1..4
+  int start[4];   // start[0] = 0, increasing
+  int stride;
+};
+
+__device__ __forceinline__ int seg_offset(const SegMap& m, int row) {
+  int k = 0;
+#pragma unroll
+  for (int i = 1; i < 4; ++i) k += (i < m.count && row >= m.start[i]) ? 1 : 0;
+  return k * m.stride;
+}
+
 // NV = ceil(d / (8 * 128)) 16-byte vectors per thread: the row's register
 // copy is sized to the actual width.  The kernel is latency-bound on its two
 // block reductions, so resident rows per SM set its bandwidth: up to NV = 5
@@ -62,9 +79,17 @@ __global__ void __launch_bounds__(kRowThreads, row_min_blocks<NV>())
     gate_adaln_kernel(__nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ branch,
                       const float* __restrict__ gate, const float* __restrict__ shift,
                       const float* __restrict__ scale, __nv_bfloat16* __restrict__ h,
-                      float* __restrict__ hs, int d, float eps) {
+                      float* __restrict__ hs, int d, float eps, SegMap sm) {
   __shared__ float red[4];
   const size_t row = blockIdx.x;
+  if (sm.count > 1) {
+    const int so = seg_offset(sm, static_cast<int>(row));
+    if (GATE) gate += so;
+    if (NORM) {
+      shift += so;
+      scale += so;
+    }
+  }
   const int nvec = d >> 3;
   uint4* xr = reinterpret_cast<uint4*>(x + row * d);
   const uint4* br = reinterpret_cast<const uint4*>(branch + (GATE ? row * d : 0));

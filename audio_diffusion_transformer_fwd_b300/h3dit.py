@@ -27,6 +27,7 @@ _EXPORTS = [
     "h3dit_last_error", "h3dit_version", "h3dit_check_device_error",
     "h3dit_timing_enable", "h3dit_timing_reset", "h3dit_timing_read",
     "h3dit_workspace_size", "h3dit_block_forward", "h3dit_block_forward_noalloc", "h3dit_step_forward",
+    "h3dit_block_forward_seg", "h3dit_step_forward_seg",
     "h3dit_quantize_act", "h3dit_quantize_weight",
     "h3dit_reduced_tokens", "h3dit_token_reduce", "h3dit_token_restore", "h3dit_reduced_positions",
     "h3dit_adaln", "h3dit_gate_residual_adaln", "h3dit_rope_table", "h3dit_qkv_project",
@@ -58,6 +59,10 @@ class VideoGrid(ctypes.Structure):
     _fields_ = [("offset", ctypes.c_int), ("T", ctypes.c_int), ("Hh", ctypes.c_int), ("W", ctypes.c_int)]
 
 
+class Segments(ctypes.Structure):
+    _fields_ = [("count", ctypes.c_int), ("start", ctypes.c_int * 4)]
+
+
 class Reduction(ctypes.Structure):
     _fields_ = [("grid", VideoGrid), ("reduce_after_block", ctypes.c_int),
                 ("restore_before_block", ctypes.c_int), ("pos_reduced", ctypes.c_void_p)]
@@ -87,6 +92,9 @@ def lib():
             "h3dit_block_forward": (i, [P(Config), P(BlockWeights), vp, vp, vp, i, vp, sz, vp]),
             "h3dit_block_forward_noalloc": (i, [P(Config), P(BlockWeights), vp, vp, vp, i, vp]),
             "h3dit_step_forward": (i, [P(Config), P(BlockWeights), i, vp, vp, vp, i, P(Reduction), vp, sz, vp]),
+            "h3dit_block_forward_seg": (i, [P(Config), P(BlockWeights), vp, P(Segments), vp, vp, i, vp, sz, vp]),
+            "h3dit_step_forward_seg": (i, [P(Config), P(BlockWeights), i, vp, P(Segments), vp, vp, i, P(Reduction),
+                                           vp, sz, vp]),
             "h3dit_quantize_act": (i, [vp, i, i, i, vp, vp, vp]),
             "h3dit_quantize_weight": (i, [vp, i, i, vp, vp, vp]),
             "h3dit_reduced_tokens": (i, [i, P(VideoGrid)]),
@@ -232,6 +240,29 @@ def h3dit_step_forward(shape: BlockShape, ws_list: Sequence[BlockWeights], mods,
     _check(lib().h3dit_step_forward(ctypes.byref(shape.c()), arr, len(ws_list), _ptr(mods), _ptr(x), _ptr(pos),
                                     n_tokens, ctypes.byref(tr) if tr is not None else None, _ptr(ws),
                                     ws_bytes, _stream(stream)))
+
+
+def segments(starts: Sequence[int]) -> Segments:
+    """Segment table from the first row of each segment (starts[0] = 0)."""
+    sg = Segments()
+    sg.count = len(starts)
+    for k, v in enumerate(starts):
+        sg.start[k] = int(v)
+    return sg
+
+
+def h3dit_block_forward_seg(shape: BlockShape, w: BlockWeights, mods, seg: Segments, x, pos, n_tokens: int, ws,
+                            ws_bytes: int, stream=None):
+    _check(lib().h3dit_block_forward_seg(ctypes.byref(shape.c()), ctypes.byref(w), _ptr(mods), ctypes.byref(seg),
+                                         _ptr(x), _ptr(pos), n_tokens, _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def h3dit_step_forward_seg(shape: BlockShape, ws_list: Sequence[BlockWeights], mods, seg: Segments, x, pos,
+                           n_tokens: int, tr: Optional[Reduction], ws, ws_bytes: int, stream=None):
+    arr = (BlockWeights * len(ws_list))(*ws_list)
+    _check(lib().h3dit_step_forward_seg(ctypes.byref(shape.c()), arr, len(ws_list), _ptr(mods), ctypes.byref(seg),
+                                        _ptr(x), _ptr(pos), n_tokens, ctypes.byref(tr) if tr is not None else None,
+                                        _ptr(ws), ws_bytes, _stream(stream)))
 
 
 def h3dit_quantize_act(x, rows: int, cols: int, group: int, q, scales, stream=None):

@@ -131,6 +131,18 @@ typedef struct {
   const float* pos_reduced;
 } h3dit_reduction;
 
+/* Consecutive token segments with their own AdaLN modulation ([linlog]
+ * "音频处理": the reference audio is conditioned at its own timestep, 1.0, so
+ * its precomputed AdaLN vectors differ from the video's).  Segment k covers
+ * rows start[k] .. start[k+1]-1 (the last runs to the end); 1 <= count <= 4,
+ * start[0] = 0, starts increasing.  With a token reduction every boundary
+ * must lie outside the paired video grid (both members of a pair share a
+ * segment); boundaries after the grid move up with the rows it removes. */
+typedef struct {
+  int count;
+  int start[4];
+} h3dit_segments;
+
 /* ---------------------------------------------------------------- housekeeping */
 
 /* Message of the last failed call on this thread ("" if none).  The string
@@ -199,6 +211,26 @@ h3dit_status h3dit_step_forward(const h3dit_config* cfg, const h3dit_block_weigh
                                 int n_blocks, const float* mods, void* x, const float* pos,
                                 int n_tokens, const h3dit_reduction* tr, void* ws,
                                 size_t ws_bytes, cudaStream_t stream);
+
+/* h3dit_block_forward with per-segment modulation: mods is device fp32
+ * [seg->count][6][d], segment k's shift1, scale1, gate1, shift2, scale2, gate2
+ * applying to its rows (AdaLN-1, the gates and AdaLN-2 all take the row's
+ * segment vectors).  seg: host pointer, read during the call.  count = 1
+ * with mods [1][6][d] is h3dit_block_forward.  E_INVAL for a malformed
+ * segment table. */
+h3dit_status h3dit_block_forward_seg(const h3dit_config* cfg, const h3dit_block_weights* w,
+                                     const float* mods, const h3dit_segments* seg, void* x,
+                                     const float* pos, int n_tokens, void* ws, size_t ws_bytes,
+                                     cudaStream_t stream);
+
+/* h3dit_step_forward with per-segment modulation: mods is device fp32
+ * [n_blocks][seg->count][6][d]; the segment boundaries are given at full
+ * resolution and follow the token reduction as h3dit_segments says. */
+h3dit_status h3dit_step_forward_seg(const h3dit_config* cfg, const h3dit_block_weights* w,
+                                    int n_blocks, const float* mods, const h3dit_segments* seg,
+                                    void* x, const float* pos, int n_tokens,
+                                    const h3dit_reduction* tr, void* ws, size_t ws_bytes,
+                                    cudaStream_t stream);
 
 /* The block of h3dit_block_forward for callers that cannot allocate device
  * memory or hand over a workspace (for instance a host program whose single

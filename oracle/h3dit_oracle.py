@@ -57,7 +57,7 @@ import numpy as np
 __all__ = [
     "BlockConfig", "VideoGrid", "Reduction",
     "bf16_round", "layer_norm", "adaln", "rope_angles", "apply_rope",
-    "attention", "gelu_tanh", "block_forward", "step_forward",
+    "attention", "gelu_tanh", "block_forward", "step_forward", "segment_mod",
     "quantize_rows", "quantize_weight", "gemm_int", "linear_int8", "INT8_ALL", "INT8_MLP", "INT8_QKV",
     "fc2_int8", "block_forward_int8",
     "reduced_token_count", "token_reduce", "token_restore",
@@ -240,13 +240,40 @@ def _merge_heads(t) -> np.ndarray:
     return t.transpose(1, 0, 2).reshape(n, h * dh)
 
 
+def segment_mod(mod_seg, starts, n_tokens: int) -> np.ndarray:
+    """Per-token modulation [6, N, d] from per-segment vectors.
+
+    [linlog] "音频处理": the reference audio is conditioned at its own timestep
+    (1.0), so its precomputed AdaLN vectors differ from the video's; each
+    segment of consecutive tokens has its own [6, d] set.  mod_seg [S, 6, d];
+    segment s covers tokens starts[s] .. starts[s+1]-1 (starts[0] = 0, the
+    last segment runs to the end)."""
+    mod_seg = np.asarray(mod_seg, dtype=np.float64)
+    starts = list(starts) + [n_tokens]
+    assert starts[0] == 0 and len(starts) == mod_seg.shape[0] + 1
+    seg = np.zeros(n_tokens, dtype=np.int64)
+    for s_ in range(mod_seg.shape[0]):
+        seg[starts[s_]:starts[s_ + 1]] = s_
+    return mod_seg[seg].transpose(1, 0, 2)
+
+
+def _mod_parts(mod, sel):
+    """(shift1, scale1, gate1, shift2, scale2, gate2) of a [6, d] or per-token
+    [6, N, d] modulation; the last four restricted to the rows ``sel``."""
+    mod = np.asarray(mod, dtype=np.float64)
+    shift1, scale1, gate1, shift2, scale2, gate2 = mod
+    if mod.ndim == 3:
+        gate1, shift2, scale2, gate2 = (v[sel] for v in (gate1, shift2, scale2, gate2))
+    return shift1, scale1, gate1, shift2, scale2, gate2
+
+
 def block_forward(x, w: Dict[str, np.ndarray], mod, pos, cfg: BlockConfig,
                   bf16_storage: bool = False, rows=None, return_parts: bool = False):
     """One dense single-stream DiT block, fp64.
 
     x [N, d]; w: w_qkv [3d, d], w_o [d, d], w1 [F, d], w2 [d, F] (rows are
     output channels); mod [6, d] = shift1, scale1, gate1, shift2, scale2,
-    gate2; pos [N, 3].
+    gate2, or per token [6, N, d] (``segment_mod``); pos [N, 3].
 
     Steps ([linlog] "DiT 融合内核" names the gated-AdaLN pairs; [alphalab]
     the full attention):
@@ -262,15 +289,14 @@ def block_forward(x, w: Dict[str, np.ndarray], mod, pos, cfg: BlockConfig,
     those query rows (keys and values still come from every token)."""
     R = lambda a: _maybe_round(a, bf16_storage)
     x = np.asarray(x, dtype=np.float64)
-    mod = np.asarray(mod, dtype=np.float64)
-    shift1, scale1, gate1, shift2, scale2, gate2 = mod
+    sel = slice(None) if rows is None else np.asarray(rows)
+    shift1, scale1, gate1, shift2, scale2, gate2 = _mod_parts(mod, sel)
     d = cfg.d
     h = R(adaln(x, shift1, scale1, cfg.eps))
     qkv = h @ np.asarray(w["w_qkv"], np.float64).T
     q = R(apply_rope(_split_heads(qkv[:, 0:d], cfg).transpose(1, 0, 2), pos, cfg)).transpose(1, 0, 2)
     k = R(apply_rope(_split_heads(qkv[:, d:2 * d], cfg).transpose(1, 0, 2), pos, cfg)).transpose(1, 0, 2)
     v = R(_split_heads(qkv[:, 2 * d:3 * d], cfg))
-    sel = slice(None) if rows is None else np.asarray(rows)
     o = R(_merge_heads(attention(q, k, v, rows=rows)))
     a = R(o @ np.asarray(w["w_o"], np.float64).T)
     x1 = R(x[sel] + gate1 * a)
@@ -362,21 +388,37 @@ def reduced_positions(pos, grid: VideoGrid) -> np.ndarray:
 # the denoiser step ([alphalab] 50 layers; [linlog] AdaLN precomputed per
 # block, token reduction boundaries)
 # --------------------------------------------------------------------------
+def _reduce_mod_rows(mod, grid: VideoGrid, n_tokens: int):
+    """A per-token modulation [6, N, d] for the reduced sequence: each
+    reduced token takes its first member's vectors (members of a pair are
+    adjacent video tokens of one segment).  [6, d] passes through."""
+    mod = np.asarray(mod, dtype=np.float64)
+    if mod.ndim == 2:
+        return mod
+    first = [g[0] for g in _reduce_map(n_tokens, grid)]
+    return mod[:, first, :]
+
+
 def step_forward(x, weights: List[Dict[str, np.ndarray]], mods, pos, cfg: BlockConfig,
                  reduction: Optional[Reduction] = None, bf16_storage: bool = False,
-                 int8: bool = False):
-    """Run the blocks in order with their own weights and modulation.  With a
-    reduction, the sequence is reduced after block ``reduce_after_block`` and
-    restored before block ``restore_before_block``."""
+                 int8: bool = False, which=None):
+    """Run the blocks in order with their own weights and modulation (each
+    [6, d] or per token [6, N, d] at full resolution).  With a reduction, the
+    sequence is reduced after block ``reduce_after_block`` and restored
+    before block ``restore_before_block``."""
     x = np.asarray(x, dtype=np.float64)
     pos = np.asarray(pos, dtype=np.float64)
+    n_full = x.shape[0]
     cur, cur_pos, side = x, pos, None
     for b, (w, mod) in enumerate(zip(weights, mods)):
         if reduction is not None and side is not None and b == reduction.restore_before_block:
             cur = token_restore(cur, side, reduction.grid, bf16_storage)
             cur_pos, side = pos, None
+        if side is not None:
+            mod = _reduce_mod_rows(mod, reduction.grid, n_full)
         if int8:
-            cur = block_forward_int8(cur, w, mod, cur_pos, cfg, bf16_storage=bf16_storage)
+            cur = block_forward_int8(cur, w, mod, cur_pos, cfg, bf16_storage=bf16_storage,
+                                     which=INT8_ALL if which is None else which)
         else:
             cur = block_forward(cur, w, mod, cur_pos, cfg, bf16_storage=bf16_storage)
         if (reduction is not None and b == reduction.reduce_after_block
@@ -478,8 +520,8 @@ def block_forward_int8(x, w: Dict[str, np.ndarray], mod, pos, cfg: BlockConfig,
     and values exist)."""
     R = lambda a: _maybe_round(a, bf16_storage)
     x = np.asarray(x, dtype=np.float64)
-    mod = np.asarray(mod, dtype=np.float64)
-    shift1, scale1, gate1, shift2, scale2, gate2 = mod
+    sel = slice(None) if rows is None else np.asarray(rows)
+    shift1, scale1, gate1, shift2, scale2, gate2 = _mod_parts(mod, sel)
     d = cfg.d
     f = cfg.ffn
     g2 = min(fc2_group, f)
@@ -493,7 +535,6 @@ def block_forward_int8(x, w: Dict[str, np.ndarray], mod, pos, cfg: BlockConfig,
     q = R(apply_rope(_split_heads(qkv[:, 0:d], cfg).transpose(1, 0, 2), pos, cfg)).transpose(1, 0, 2)
     k = R(apply_rope(_split_heads(qkv[:, d:2 * d], cfg).transpose(1, 0, 2), pos, cfg)).transpose(1, 0, 2)
     v = R(_split_heads(qkv[:, 2 * d:3 * d], cfg))
-    sel = slice(None) if rows is None else np.asarray(rows)
     o = R(_merge_heads(attention(q, k, v, rows=rows)))
     if "o" in which:
         oq, os_ = quantize_rows(o)
