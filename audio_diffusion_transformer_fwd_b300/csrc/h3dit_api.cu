@@ -15,6 +15,7 @@
 
 #include "../../include/h3dit.h"
 #include "attention.cuh"
+#include "final.cuh"
 #include "gemm.cuh"
 #include "gemm_i8.cuh"
 #include "ptx.cuh"
@@ -1014,6 +1015,69 @@ h3dit_status h3dit_qkv_project_i8(const h3dit_config* cfg, const void* hq, const
   g.rope = reinterpret_cast<const float2*>(table);
   return launch_gemm_i8(h3::kEpiQKV, hq, hs, cfg->d, w_qkv, s_qkv, n_tokens, 3 * cfg->d, cfg->d, g, nullptr, kQKV,
                         stream);
+}
+
+h3dit_status h3dit_final_layer(const h3dit_config* cfg, const void* x, int n_tokens, const h3dit_final_head* heads,
+                               int n_heads, cudaStream_t stream) {
+  H3_TRY(check_cfg(cfg));
+  if (!x || !heads) return fail(H3DIT_E_INVAL, "NULL pointer");
+  if (n_tokens < 1) return fail(H3DIT_E_INVAL, "n_tokens %d", n_tokens);
+  if (n_heads < 1 || n_heads > 4) return fail(H3DIT_E_INVAL, "n_heads %d (1..4)", n_heads);
+  if (!aligned(x, 16)) return fail(H3DIT_E_INVAL, "x must be 16-byte aligned");
+  const int d = cfg->d;
+  for (int i = 0; i < n_heads; ++i) {
+    const h3dit_final_head& h = heads[i];
+    if (!h.shift || !h.scale || !h.w || !h.out) return fail(H3DIT_E_INVAL, "head %d has a NULL pointer", i);
+    if (h.rows < 1 || h.row_start < 0 || h.row_start + h.rows > n_tokens)
+      return fail(H3DIT_E_INVAL, "head %d rows %d..%d outside the %d tokens", i, h.row_start, h.row_start + h.rows,
+                  n_tokens);
+    if (h.c_out < 16 || h.c_out > h3::kHeadMaxN || h.c_out % 16 != 0)
+      return fail(H3DIT_E_UNSUPPORTED, "head %d c_out %d (a multiple of 16, 16..256)", i, h.c_out);
+    if (!aligned(h.w, 16) || !aligned(h.out, 16) || !aligned(h.shift, 16) || !aligned(h.scale, 16))
+      return fail(H3DIT_E_INVAL, "head %d tensors must be 16-byte aligned", i);
+  }
+  static bool once = false;
+  if (!once) {
+    H3_TRY(set_smem(h3::final_head_kernel, h3::kHeadSmemLimit + 1536));
+    once = true;
+  }
+  h3::HeadBatch hb{};
+  {
+    const uint64_t dims[2] = {(uint64_t)d, (uint64_t)n_tokens};
+    const uint64_t str[1] = {(uint64_t)d * 2};
+    const uint32_t box[2] = {h3::kHeadBK, 128};
+    H3_TRY(make_map(&hb.tmX, x, 2, dims, str, box));
+  }
+  int max_tiles = 0;
+  size_t smem = 0;
+  TimedLaunch tl(kRows, stream);
+  for (int i = 0; i < n_heads; ++i) {
+    const h3dit_final_head& h = heads[i];
+    const uint64_t dims[2] = {(uint64_t)d, (uint64_t)h.c_out};
+    const uint64_t str[1] = {(uint64_t)d * 2};
+    const uint32_t box[2] = {h3::kHeadBK, (uint32_t)h.c_out};
+    H3_TRY(make_map(&hb.tmW[i], h.w, 2, dims, str, box));
+    h3::HeadArgs& a = hb.a[i];
+    a.row_start = h.row_start;
+    a.rows = h.rows;
+    a.d = d;
+    a.shift = h.shift;
+    a.scale = h.scale;
+    a.c_out = h.c_out;
+    a.out = static_cast<bf16*>(h.out);
+    uint32_t cols = 32;
+    while (cols < (uint32_t)h.c_out) cols <<= 1;
+    a.tmem_cols = cols;
+    a.stages = h3::head_stages(h.c_out);
+    max_tiles = std::max(max_tiles, (h.rows + 127) / 128);
+    smem = std::max(smem, h3::head_smem_bytes(h.c_out));
+    h3::head_stats_kernel<<<(h.rows * 32 + 255) / 256, 256, 0, stream>>>(static_cast<const bf16*>(x), h.row_start,
+                                                                         h.rows, d, cfg->eps, a.out, h.c_out);
+    H3_CUDA(cudaGetLastError());
+  }
+  h3::final_head_kernel<<<dim3(max_tiles, n_heads), h3::kHeadThreads, smem, stream>>>(hb);
+  H3_CUDA(cudaGetLastError());
+  return H3DIT_OK;
 }
 
 int h3dit_reduced_tokens(int n_tokens, const h3dit_video_grid* g) {

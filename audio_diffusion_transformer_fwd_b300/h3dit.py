@@ -27,7 +27,7 @@ _EXPORTS = [
     "h3dit_last_error", "h3dit_version", "h3dit_check_device_error",
     "h3dit_timing_enable", "h3dit_timing_reset", "h3dit_timing_read",
     "h3dit_workspace_size", "h3dit_block_forward", "h3dit_block_forward_noalloc", "h3dit_step_forward",
-    "h3dit_block_forward_seg", "h3dit_step_forward_seg",
+    "h3dit_block_forward_seg", "h3dit_step_forward_seg", "h3dit_final_layer",
     "h3dit_quantize_act", "h3dit_quantize_weight",
     "h3dit_reduced_tokens", "h3dit_token_reduce", "h3dit_token_restore", "h3dit_reduced_positions",
     "h3dit_adaln", "h3dit_gate_residual_adaln", "h3dit_rope_table", "h3dit_qkv_project",
@@ -63,6 +63,11 @@ class Segments(ctypes.Structure):
     _fields_ = [("count", ctypes.c_int), ("start", ctypes.c_int * 4)]
 
 
+class FinalHead(ctypes.Structure):
+    _fields_ = [("row_start", ctypes.c_int), ("rows", ctypes.c_int), ("shift", ctypes.c_void_p),
+                ("scale", ctypes.c_void_p), ("w", ctypes.c_void_p), ("c_out", ctypes.c_int), ("out", ctypes.c_void_p)]
+
+
 class Reduction(ctypes.Structure):
     _fields_ = [("grid", VideoGrid), ("reduce_after_block", ctypes.c_int),
                 ("restore_before_block", ctypes.c_int), ("pos_reduced", ctypes.c_void_p)]
@@ -92,6 +97,7 @@ def lib():
             "h3dit_block_forward": (i, [P(Config), P(BlockWeights), vp, vp, vp, i, vp, sz, vp]),
             "h3dit_block_forward_noalloc": (i, [P(Config), P(BlockWeights), vp, vp, vp, i, vp]),
             "h3dit_step_forward": (i, [P(Config), P(BlockWeights), i, vp, vp, vp, i, P(Reduction), vp, sz, vp]),
+            "h3dit_final_layer": (i, [P(Config), vp, i, P(FinalHead), i, vp]),
             "h3dit_block_forward_seg": (i, [P(Config), P(BlockWeights), vp, P(Segments), vp, vp, i, vp, sz, vp]),
             "h3dit_step_forward_seg": (i, [P(Config), P(BlockWeights), i, vp, P(Segments), vp, vp, i, P(Reduction),
                                            vp, sz, vp]),
@@ -263,6 +269,18 @@ def h3dit_step_forward_seg(shape: BlockShape, ws_list: Sequence[BlockWeights], m
     _check(lib().h3dit_step_forward_seg(ctypes.byref(shape.c()), arr, len(ws_list), _ptr(mods), ctypes.byref(seg),
                                         _ptr(x), _ptr(pos), n_tokens, ctypes.byref(tr) if tr is not None else None,
                                         _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def final_head(row_start: int, rows: int, shift, scale, w, c_out: int, out) -> FinalHead:
+    h = FinalHead()
+    h.row_start, h.rows, h.c_out = row_start, rows, c_out
+    h.shift, h.scale, h.w, h.out = _ptr(shift), _ptr(scale), _ptr(w), _ptr(out)
+    return h
+
+
+def h3dit_final_layer(shape: BlockShape, x, n_tokens: int, heads: Sequence[FinalHead], stream=None):
+    arr = (FinalHead * len(heads))(*heads)
+    _check(lib().h3dit_final_layer(ctypes.byref(shape.c()), _ptr(x), n_tokens, arr, len(heads), _stream(stream)))
 
 
 def h3dit_quantize_act(x, rows: int, cols: int, group: int, q, scales, stream=None):

@@ -385,6 +385,9 @@ def run_ours(args):
     # ---- the same block on the dynamic-int8 path
     int8_res = run_int8_block(args, H, synth, torch, stream, barrier, max_over_ranks, rank, wdev, mod, x, pos)
 
+    # ---- the final layer (video and audio heads) on the block's output
+    final_res = run_final_layer(args, H, torch, stream, barrier, max_over_ranks, shape, x, n, d, hbm)
+
     # ---- 50-block steps (864x480 class), latency
     step_res = {}
     if not args.skip_step:
@@ -407,12 +410,52 @@ def run_ours(args):
             "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu,
             "e2e": {"value": fl * ws / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": int(launches), "clocks": clocks, "int8": int8_res, "step": step_res,
+            "gpu_launches": int(launches), "clocks": clocks, "int8": int8_res, "final_layer": final_res,
+            "step": step_res,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def run_final_layer(args, H, torch, stream, barrier, max_over_ranks, shape, x, n, d, hbm):
+    """The final layer at the 512 class: a video head over rows 0..6143 and
+    an audio head over rows 6656..6911, 64 output channels each, AdaLN fused
+    into the projection's operand load.  HBM-bound: the algorithmic bytes are
+    the head rows read once plus the weights and the outputs."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    specs = ((0, 6144, 64), (6656, 256, 64))
+    heads, keep = [], []
+    for r0, rows, c in specs:
+        sh = torch.randn(d, device="cuda", generator=g) * 0.1
+        sc = torch.randn(d, device="cuda", generator=g) * 0.1
+        wt = (torch.randn((c, d), device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+        out = torch.empty((rows, c), device="cuda", dtype=torch.bfloat16)
+        heads.append(H.final_head(r0, rows, sh, sc, wt, c, out))
+        keep += [sh, sc, wt, out]
+    # three copies of the stream (210 MB, more than L2) used in turn
+    xs = [x] + [x.clone() for _ in range(2)]
+    for i in range(args.warmup):
+        H.h3dit_final_layer(shape, xs[i % 3], n, heads, stream)
+    H.h3dit_check_device_error(stream)
+    steps = max(1, min(args.steps, 51))
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        H.h3dit_final_layer(shape, xs[i % 3], n, heads, stream)
+    e1.record(stream)
+    barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1)) / steps
+    byts = sum(rows * d * 2 + c * d * 2 + rows * c * 2 + 8 * d for _, rows, c in specs)
+    flops = sum(2.0 * rows * d * c for _, rows, c in specs)
+    return {"workload": "video head rows 0..6143 + audio head rows 6656..6911 of the 512-class stream, "
+                        "64 output channels each",
+            "ms": ms, "gbs": byts / (ms * 1e-3) / 1e9, "frac_of_hbm": byts / (ms * 1e-3) / 1e9 / hbm,
+            "tflops": flops / (ms * 1e-3) / 1e12, "bytes": byts, "steps": steps,
+            "l2": "three copies of the stream used in turn (210 MB, more than L2)"}
 
 
 def run_int8_block(args, H, synth, torch, stream, barrier, max_over_ranks, rank, wdev, mod, x, pos):

@@ -253,6 +253,35 @@ h3dit_status h3dit_block_forward_noalloc(const h3dit_config* cfg, const h3dit_bl
                                          const float* mod, void* x, const float* pos, int n_tokens,
                                          cudaStream_t stream);
 
+/* ---------------------------------------------------------------- the final layer */
+
+/* One output head of the final layer ([linlog] "DiT 融合内核": the audio and
+ * video AdaLN kernels are bound directly to residual-stream offsets, and the
+ * BF16 final head applies AdaLN while it loads its projection tiles):
+ *   out[r][c] = bf16( sum_k bf16(LN(x[row_start + r])_k (1 + scale_k) + shift_k) * w[c][k] )
+ * for r < rows, LayerNorm as in the block (biased variance, cfg->eps).
+ * shift, scale: device fp32 [d]; w: device BF16 [c_out][d]; out: device BF16
+ * [rows][c_out]; c_out a multiple of 16 in 16..256; all 16-byte aligned. */
+typedef struct {
+  int row_start;
+  int rows;
+  const float* shift;
+  const float* scale;
+  const void* w;
+  int c_out;
+  void* out;
+} h3dit_final_head;
+
+/* The final layer over up to 4 heads (e.g. video and audio rows of the
+ * residual stream x, device BF16 [n_tokens][d]).  x is only read; no
+ * workspace and no normalised copy of the rows is made: each output row
+ * first holds its row's LayerNorm statistics (8 bytes), then the result, so
+ * an output must not overlap x or another head's output.  heads: host array,
+ * read during the call.  Errors: E_INVAL (nulls, rows outside x, more than 4
+ * heads), E_UNSUPPORTED (c_out), E_CUDA. */
+h3dit_status h3dit_final_layer(const h3dit_config* cfg, const void* x, int n_tokens,
+                               const h3dit_final_head* heads, int n_heads, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- quantisation */
 
 /* Dynamic symmetric int8 quantisation ([linlog] "int8 量化": activations

@@ -57,7 +57,7 @@ import numpy as np
 __all__ = [
     "BlockConfig", "VideoGrid", "Reduction",
     "bf16_round", "layer_norm", "adaln", "rope_angles", "apply_rope",
-    "attention", "gelu_tanh", "block_forward", "step_forward", "segment_mod",
+    "attention", "gelu_tanh", "block_forward", "step_forward", "segment_mod", "final_head",
     "quantize_rows", "quantize_weight", "gemm_int", "linear_int8", "INT8_ALL", "INT8_MLP", "INT8_QKV",
     "fc2_int8", "block_forward_int8",
     "reduced_token_count", "token_reduce", "token_restore",
@@ -316,6 +316,21 @@ def block_flops(n: int, cfg: BlockConfig) -> float:
     gemm = 2.0 * n * d * (3 * d) + 2.0 * n * d * d + 2.0 * n * d * f * 2
     attn = 4.0 * n * n * d
     return gemm + attn
+
+
+# --------------------------------------------------------------------------
+# final layer ([linlog] "DiT 融合内核": final-layer binding)
+# --------------------------------------------------------------------------
+def final_head(x, row_start: int, rows: int, shift, scale, w, eps: float, bf16_storage: bool = False):
+    """One output head of the final layer: the rows row_start .. row_start +
+    rows - 1 of the residual stream, normalised with the head's own AdaLN
+    vectors (the audio and video heads read their rows in place), projected
+    by w [c_out, d]: out = AdaLN(x[rows]) w^T.  ``bf16_storage`` rounds the
+    normalised operand and the output to BF16, as a BF16 head does."""
+    R = lambda a: _maybe_round(a, bf16_storage)
+    xs = np.asarray(x, dtype=np.float64)[row_start:row_start + rows]
+    h = R(adaln(xs, np.asarray(shift, np.float64), np.asarray(scale, np.float64), eps))
+    return R(h @ np.asarray(w, np.float64).T)
 
 
 # --------------------------------------------------------------------------

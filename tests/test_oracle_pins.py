@@ -568,3 +568,31 @@ def test_step_reduction_with_segments():
     y2 = O.block_forward(y2, w, per_row, pos, cfg)
     assert np.allclose(got, y2, atol=1e-13)
 
+
+# ------------------------------------------------------------------ final layer
+
+
+def test_final_head_identity_projection_is_layer_norm():
+    """With zero shift/scale and the identity as projection the head returns
+    the textbook LayerNorm of its rows (torch, fp64)."""
+    r = np.random.default_rng(20)
+    x = r.standard_normal((30, 48)) * 3 + 1
+    got = O.final_head(x, 5, 20, np.zeros(48), np.zeros(48), np.eye(48), 1e-6)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(x[5:25]), (48,), eps=1e-6).numpy()
+    assert np.allclose(got, ref, atol=1e-12)
+
+
+def test_final_head_scalar_loops():
+    r = np.random.default_rng(21)
+    n, d, c = 9, 16, 5
+    x = r.standard_normal((n, d))
+    sh, sc, w = r.standard_normal(d) * 0.2, r.standard_normal(d) * 0.2, r.standard_normal((c, d))
+    got = O.final_head(x, 2, 4, sh, sc, w, 1e-6)
+    for i in range(4):
+        row = x[2 + i]
+        mu = sum(row) / d
+        var = sum((v - mu) ** 2 for v in row) / d
+        hrow = [(row[k] - mu) / math.sqrt(var + 1e-6) * (1 + sc[k]) + sh[k] for k in range(d)]
+        for o in range(c):
+            assert abs(got[i, o] - sum(hrow[k] * w[o, k] for k in range(d))) < 1e-12
+
