@@ -1080,6 +1080,35 @@ h3dit_status h3dit_final_layer(const h3dit_config* cfg, const void* x, int n_tok
   return H3DIT_OK;
 }
 
+h3dit_status h3dit_core_residual(const void* x_in, const void* x_out, size_t count, float* delta,
+                                 cudaStream_t stream) {
+  if (!x_in || !x_out || !delta) return fail(H3DIT_E_INVAL, "NULL pointer");
+  if (count == 0) return H3DIT_OK;
+  if (count % 8 != 0) return fail(H3DIT_E_UNSUPPORTED, "count %zu (multiple of 8)", count);
+  if (!aligned(x_in, 16) || !aligned(x_out, 16) || !aligned(delta, 16))
+    return fail(H3DIT_E_INVAL, "tensors must be 16-byte aligned");
+  const size_t n8 = count / 8, blocks = (n8 + 255) / 256;
+  if (blocks > 0x7fffffffULL) return fail(H3DIT_E_UNSUPPORTED, "count %zu too large", count);
+  TimedLaunch tl(kRows, stream);
+  h3::core_residual_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const bf16*>(x_in),
+                                                                  static_cast<const bf16*>(x_out), n8, delta);
+  H3_CUDA(cudaGetLastError());
+  return H3DIT_OK;
+}
+
+h3dit_status h3dit_core_reuse(void* x, const float* delta, size_t count, cudaStream_t stream) {
+  if (!x || !delta) return fail(H3DIT_E_INVAL, "NULL pointer");
+  if (count == 0) return H3DIT_OK;
+  if (count % 8 != 0) return fail(H3DIT_E_UNSUPPORTED, "count %zu (multiple of 8)", count);
+  if (!aligned(x, 16) || !aligned(delta, 16)) return fail(H3DIT_E_INVAL, "tensors must be 16-byte aligned");
+  const size_t n8 = count / 8, blocks = (n8 + 255) / 256;
+  if (blocks > 0x7fffffffULL) return fail(H3DIT_E_UNSUPPORTED, "count %zu too large", count);
+  TimedLaunch tl(kRows, stream);
+  h3::core_reuse_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<bf16*>(x), delta, n8);
+  H3_CUDA(cudaGetLastError());
+  return H3DIT_OK;
+}
+
 int h3dit_reduced_tokens(int n_tokens, const h3dit_video_grid* g) {
   if (!g || check_grid(g, n_tokens) != H3DIT_OK) return -1;
   return pair_grid(g, n_tokens).n_red;

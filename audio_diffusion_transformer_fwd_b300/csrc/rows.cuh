@@ -274,6 +274,35 @@ __global__ void __launch_bounds__(kRowThreads)
   }
 }
 
+// Core residual reuse ([linlog] speed/quality presets, "--core-reuse"):
+// delta = x_out - x_in in fp32 (exact for BF16 streams whose exponents are
+// within 16 of each other), and a reuse step x = bf16(x + delta).  Eight
+// elements per thread, 16-byte loads.
+__global__ void core_residual_kernel(const __nv_bfloat16* __restrict__ x_in, const __nv_bfloat16* __restrict__ x_out,
+                                     size_t n8, float* __restrict__ delta) {
+  const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  float a[8], b[8];
+  unpack8(reinterpret_cast<const uint4*>(x_in)[i], a);
+  unpack8(reinterpret_cast<const uint4*>(x_out)[i], b);
+  float4* o = reinterpret_cast<float4*>(delta) + 2 * i;
+  o[0] = make_float4(b[0] - a[0], b[1] - a[1], b[2] - a[2], b[3] - a[3]);
+  o[1] = make_float4(b[4] - a[4], b[5] - a[5], b[6] - a[6], b[7] - a[7]);
+}
+
+__global__ void core_reuse_kernel(__nv_bfloat16* __restrict__ x, const float* __restrict__ delta, size_t n8) {
+  const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  float a[8];
+  unpack8(reinterpret_cast<const uint4*>(x)[i], a);
+  const float4 d0 = reinterpret_cast<const float4*>(delta)[2 * i];
+  const float4 d1 = reinterpret_cast<const float4*>(delta)[2 * i + 1];
+  const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+  for (int e = 0; e < 8; ++e) a[e] += dd[e];
+  reinterpret_cast<uint4*>(x)[i] = pack8(a);
+}
+
 // Row maps of the horizontal-pair reduction.  Full row i -> reduced row.
 struct PairGrid {
   int offset, T, Hh, W, Wr;   // Wr = ceil(W/2)

@@ -27,7 +27,8 @@ _EXPORTS = [
     "h3dit_last_error", "h3dit_version", "h3dit_check_device_error",
     "h3dit_timing_enable", "h3dit_timing_reset", "h3dit_timing_read",
     "h3dit_workspace_size", "h3dit_block_forward", "h3dit_block_forward_noalloc", "h3dit_step_forward",
-    "h3dit_block_forward_seg", "h3dit_step_forward_seg", "h3dit_final_layer",
+    "h3dit_block_forward_seg", "h3dit_step_forward_seg", "h3dit_final_layer", "h3dit_core_residual",
+    "h3dit_core_reuse",
     "h3dit_quantize_act", "h3dit_quantize_weight",
     "h3dit_reduced_tokens", "h3dit_token_reduce", "h3dit_token_restore", "h3dit_reduced_positions",
     "h3dit_adaln", "h3dit_gate_residual_adaln", "h3dit_rope_table", "h3dit_qkv_project",
@@ -98,6 +99,8 @@ def lib():
             "h3dit_block_forward_noalloc": (i, [P(Config), P(BlockWeights), vp, vp, vp, i, vp]),
             "h3dit_step_forward": (i, [P(Config), P(BlockWeights), i, vp, vp, vp, i, P(Reduction), vp, sz, vp]),
             "h3dit_final_layer": (i, [P(Config), vp, i, P(FinalHead), i, vp]),
+            "h3dit_core_residual": (i, [vp, vp, sz, vp, vp]),
+            "h3dit_core_reuse": (i, [vp, vp, sz, vp]),
             "h3dit_block_forward_seg": (i, [P(Config), P(BlockWeights), vp, P(Segments), vp, vp, i, vp, sz, vp]),
             "h3dit_step_forward_seg": (i, [P(Config), P(BlockWeights), i, vp, P(Segments), vp, vp, i, P(Reduction),
                                            vp, sz, vp]),
@@ -281,6 +284,14 @@ def final_head(row_start: int, rows: int, shift, scale, w, c_out: int, out) -> F
 def h3dit_final_layer(shape: BlockShape, x, n_tokens: int, heads: Sequence[FinalHead], stream=None):
     arr = (FinalHead * len(heads))(*heads)
     _check(lib().h3dit_final_layer(ctypes.byref(shape.c()), _ptr(x), n_tokens, arr, len(heads), _stream(stream)))
+
+
+def h3dit_core_residual(x_in, x_out, count: int, delta, stream=None):
+    _check(lib().h3dit_core_residual(_ptr(x_in), _ptr(x_out), count, _ptr(delta), _stream(stream)))
+
+
+def h3dit_core_reuse(x, delta, count: int, stream=None):
+    _check(lib().h3dit_core_reuse(_ptr(x), _ptr(delta), count, _stream(stream)))
 
 
 def h3dit_quantize_act(x, rows: int, cols: int, group: int, q, scales, stream=None):

@@ -282,6 +282,23 @@ typedef struct {
 h3dit_status h3dit_final_layer(const h3dit_config* cfg, const void* x, int n_tokens,
                                const h3dit_final_head* heads, int n_heads, cudaStream_t stream);
 
+/* ---------------------------------------------------------------- core residual reuse */
+
+/* The speed/quality presets of [linlog] (the preset table: "--core-reuse k"
+ * refreshes the patch and head every step but runs the block core less
+ * often; "--layers" is n_blocks of h3dit_step_forward; the later restore
+ * point is restore_before_block of h3dit_reduction).  A caller runs the core
+ * (h3dit_step_forward) on a fresh step and keeps its residual; on a reuse
+ * step it adds that residual instead of running the blocks.
+ * h3dit_core_residual: delta[i] = x_out[i] - x_in[i] in fp32 (exact when the
+ *   two BF16 values' exponents are within 16 of each other).
+ * h3dit_core_reuse: x[i] = bf16(x[i] + delta[i]), in place.
+ * x_in, x_out, x: device BF16; delta: device fp32; count elements, a multiple
+ * of 8; all 16-byte aligned. */
+h3dit_status h3dit_core_residual(const void* x_in, const void* x_out, size_t count, float* delta,
+                                 cudaStream_t stream);
+h3dit_status h3dit_core_reuse(void* x, const float* delta, size_t count, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- quantisation */
 
 /* Dynamic symmetric int8 quantisation ([linlog] "int8 量化": activations

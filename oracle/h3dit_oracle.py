@@ -57,7 +57,7 @@ import numpy as np
 __all__ = [
     "BlockConfig", "VideoGrid", "Reduction",
     "bf16_round", "layer_norm", "adaln", "rope_angles", "apply_rope",
-    "attention", "gelu_tanh", "block_forward", "step_forward", "segment_mod", "final_head",
+    "attention", "gelu_tanh", "block_forward", "step_forward", "segment_mod", "final_head", "core_residual", "core_reuse",
     "quantize_rows", "quantize_weight", "gemm_int", "linear_int8", "INT8_ALL", "INT8_MLP", "INT8_QKV",
     "fc2_int8", "block_forward_int8",
     "reduced_token_count", "token_reduce", "token_restore",
@@ -331,6 +331,21 @@ def final_head(x, row_start: int, rows: int, shift, scale, w, eps: float, bf16_s
     xs = np.asarray(x, dtype=np.float64)[row_start:row_start + rows]
     h = R(adaln(xs, np.asarray(shift, np.float64), np.asarray(scale, np.float64), eps))
     return R(h @ np.asarray(w, np.float64).T)
+
+
+# --------------------------------------------------------------------------
+# core residual reuse ([linlog] speed/quality preset table, "--core-reuse":
+# every step refreshes the patch and head, the block core runs less often)
+# --------------------------------------------------------------------------
+def core_residual(x_in, x_out) -> np.ndarray:
+    """The core's residual, x_out - x_in, kept at full precision."""
+    return np.asarray(x_out, np.float64) - np.asarray(x_in, np.float64)
+
+
+def core_reuse(x, delta, bf16_storage: bool = True) -> np.ndarray:
+    """A reuse step: the core's cached residual added to this step's core
+    input in place of running the blocks; the stream stays BF16."""
+    return _maybe_round(np.asarray(x, np.float64) + np.asarray(delta, np.float64), bf16_storage)
 
 
 # --------------------------------------------------------------------------

@@ -173,3 +173,37 @@ def test_step_reduction_zero_gates_is_identity_bit_exact():
     tr = H.reduction(H.video_grid(0, T, Hh, W), 1, 4)
     got = _run_step(w, x, wts, mods, pos, tr)
     assert np.array_equal(got, x)
+
+
+def test_core_reuse_replays_a_step():
+    """Core residual reuse (the '--core-reuse' preset): the residual of a
+    2-block step, re-added to the same input, reproduces the step bit for
+    bit; added to another input it matches the oracle's BF16 sum."""
+    w = TINY
+    n = w.n_tokens
+    shape = shape_of(w)
+    pos = dev_f32(synth.positions(w.video, w.n_text, w.n_audio))
+    x = synth.host_activations(n, w.d, seed=51)
+    wts = [synth.host_block_weights(w.d, w.ffn, seed=51, block=b) for b in range(2)]
+    mods = np.stack([synth.host_mod(w.d, seed=51, block=b) for b in range(2)])
+    devs = [_weights_dev(t) for t in wts]
+    nbytes = H.h3dit_workspace_size(shape, n)
+    ws = torch.empty(nbytes, device="cuda", dtype=torch.uint8)
+    x_in = dev_bf16(x)
+    y = x_in.clone()
+    H.h3dit_step_forward(shape, [dv[1] for dv in devs], dev_f32(mods), y, pos, n, None, ws, nbytes)
+    delta = torch.empty((n, w.d), device="cuda", dtype=torch.float32)
+    H.h3dit_core_residual(x_in, y, n * w.d, delta)
+    z = x_in.clone()
+    H.h3dit_core_reuse(z, delta, n * w.d)
+    H.h3dit_check_device_error()
+    assert torch.equal(z, y)
+    assert np.array_equal(delta.cpu().numpy().astype(np.float64), O.core_residual(host(x_in), host(y)))
+    x2 = dev_bf16(synth.host_activations(n, w.d, seed=52))
+    ref = O.core_reuse(host(x2), delta.cpu().numpy().astype(np.float64))
+    H.h3dit_core_reuse(x2, delta, n * w.d)
+    H.h3dit_check_device_error()
+    got = host(x2)
+    # x + delta in fp32 then BF16 versus the exact sum rounded once: equal
+    # except where the fp32 sum lands on a BF16 rounding tie (double rounding)
+    assert np.mean(got != ref) < 1e-3 and max_abs(got, ref) <= 2.0 ** -7 * float(np.max(np.abs(ref)))

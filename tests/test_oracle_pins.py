@@ -596,3 +596,25 @@ def test_final_head_scalar_loops():
         for o in range(c):
             assert abs(got[i, o] - sum(hrow[k] * w[o, k] for k in range(d))) < 1e-12
 
+
+# ------------------------------------------------------------------ core residual reuse
+
+
+def test_core_reuse_replays_the_core_exactly():
+    """Reusing the residual on the same input gives the core's output bit for
+    bit (the residual of two BF16 streams is exact in fp64), and on another
+    input adds the same update."""
+    cfg = O.BlockConfig(d=64, heads=2, head_dim=32, ffn=128, rope_sections=(8, 12, 12))
+    r = np.random.default_rng(22)
+    n = 16
+    w = {"w_qkv": r.standard_normal((192, 64)) * 0.1, "w_o": r.standard_normal((64, 64)) * 0.1,
+         "w1": r.standard_normal((128, 64)) * 0.1, "w2": r.standard_normal((64, 128)) * 0.1}
+    x = O.bf16_round(r.standard_normal((n, 64)))
+    pos = r.uniform(0, 5, (n, 3))
+    mod = r.standard_normal((6, 64)) * 0.3
+    y = O.step_forward(x, [w, w], [mod, mod], pos, cfg, bf16_storage=True)
+    delta = O.core_residual(x, y)
+    assert np.array_equal(O.core_reuse(x, delta), y)
+    x2 = O.bf16_round(x + 0.25)
+    assert np.array_equal(O.core_reuse(x2, delta), O.bf16_round(x2 + (y - x)))
+
