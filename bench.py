@@ -180,6 +180,36 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+class Ranks:
+    """The replica plumbing of the bench: one process per GPU (torchrun),
+    a barrier that also drains the local device, and max-over-ranks timing,
+    so the slowest replica sets the time and `value` is the work of all
+    ranks divided by it.  `dist` is torch.distributed once initialised (NCCL
+    on GPUs, gloo in the CPU tests), or None for one process."""
+
+    def __init__(self, world_size, rank, dist=None, device="cuda"):
+        self.world_size, self.rank, self.dist, self.device = world_size, rank, dist, device
+
+    def barrier(self):
+        import torch
+        if self.dist is not None:
+            self.dist.barrier()
+        if self.device == "cuda":
+            torch.cuda.synchronize()
+
+    def max(self, v):
+        if self.dist is None:
+            return v
+        import torch
+        t = torch.tensor([v], device=self.device, dtype=torch.float64)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return t.item()
+
+    def throughput(self, work_per_rank, ms):
+        """Whole-job rate: every rank's work over the slowest rank's time."""
+        return work_per_rank * self.world_size / (ms * 1e-3)
+
+
 def dist_setup():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -266,18 +296,8 @@ def run_ours(args):
     if ws > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-        torch.cuda.synchronize()
-
-    def max_over_ranks(v):
-        if dist is None:
-            return v
-        t = torch.tensor([v], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return t.item()
+    ranks = Ranks(ws, rank, dist)
+    barrier, max_over_ranks = ranks.barrier, ranks.max
 
     burst, sustained, hbm, peak_src = measured_peaks()
     w = synth.WORKLOADS["block_512"]
@@ -322,7 +342,7 @@ def run_ours(args):
                   ("fc1", H.KC_FC1), ("fc2", H.KC_FC2))}
     launches = sum(c for _, c in per_class.values())
     fl = block_flops(n, d, f)
-    value = fl * ws / (ms * 1e-3) / 1e12
+    value = ranks.throughput(fl, ms) / 1e12
 
     gemm_ms = sum(per_class[k][0] for k in ("qkv", "out_proj", "fc1", "fc2")) / args.steps
     gemm_launch = sum(per_class[k][1] for k in ("qkv", "out_proj", "fc1", "fc2")) / args.steps
@@ -408,7 +428,7 @@ def run_ours(args):
             "config": {"workload": WORKLOAD_DESC, "parallelism": f"replicas x{ws}",
                        "l2": "inputs larger than L2: 629 MB of block weights streamed every step"},
             "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu,
-            "e2e": {"value": fl * ws / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+            "e2e": {"value": ranks.throughput(fl, e2e_ms) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": int(launches), "clocks": clocks, "int8": int8_res, "final_layer": final_res,
             "step": step_res,
