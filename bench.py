@@ -356,6 +356,7 @@ def run_ours(args):
         "fc1_gemm": {"ms": per_class["fc1"][0] / args.steps, "tflops": 2.0 * n * d * f / (per_class["fc1"][0] / args.steps * 1e-3) / 1e12},
         "fc2_gemm": {"ms": per_class["fc2"][0] / args.steps, "tflops": 2.0 * n * d * f / (per_class["fc2"][0] / args.steps * 1e-3) / 1e12},
         "attention": {"ms": attn_ms, "tflops": 4.0 * n * n * d / (attn_ms * 1e-3) / 1e12,
+                      "frac_of_sustained": 4.0 * n * n * d / (attn_ms * 1e-3) / 1e12 / sustained,
                       "frac_of_burst": 4.0 * n * n * d / (attn_ms * 1e-3) / 1e12 / burst},
         "row_kernels": {"ms": rows_ms, "note": "rope table + AdaLN-1 + gated residual fused with AdaLN-2 + "
                         "final gated residual per block"},
@@ -373,33 +374,62 @@ def run_ours(args):
         kernels["row_kernels"]["gbs"] = rows_gbs
         kernels["row_kernels"]["frac_of_hbm"] = rows_gbs / hbm
 
+    # The timed region is 200+ back-to-back blocks with the power cap engaged
+    # (see clocks), i.e. kernels inside a long step: the denominator is the
+    # measured sustained BF16 rate; the burst fraction is given beside it.
     roofline = {"kernel": "tcgen05 BF16 GEMM (QKV+RoPE, out-proj, FC1+GELU, FC2), all launches of a block",
-                "bound": "tensor", "achieved": achieved, "peak": burst, "unit": "TFLOP/s",
-                "frac": achieved / burst, "peak_source": f"{peak_src} bf16 burst (cuBLAS 8192^3)",
+                "bound": "tensor", "achieved": achieved, "peak": sustained, "unit": "TFLOP/s",
+                "frac": achieved / sustained, "frac_of_burst": achieved / burst,
+                "peak_source": f"{peak_src} bf16 sustained (cuBLAS 8192^3 back to back for 4 s under the power cap); "
+                               f"burst {burst}",
                 "traffic": ncu_traffic("gemm_per_block"), "algorithmic_flops_per_block": gfl,
                 "launches_per_block": gemm_launch}
 
-    # ---- end-to-end through the C ABI with host buffers
+    # ---- end-to-end through the C ABI with host buffers.  Every step copies
+    # its input (x, mod, pos) from pinned host memory and its result back.
+    # The copies run on their own streams and the device buffers are double
+    # buffered, so step i+1's upload and step i-1's download overlap step i's
+    # blocks -- the pipelining a serving loop would use.
     xh = torch.empty((n, d), dtype=torch.bfloat16).pin_memory()
     xh.copy_(x.cpu())
     modh = mod.cpu().pin_memory()
     posh = pos.cpu().pin_memory()
-    xo = torch.empty((n, d), dtype=torch.bfloat16).pin_memory()
+    xo = [torch.empty((n, d), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    xb = [x, x.clone()]
+    mb = [mod, mod.clone()]
+    pb = [pos, pos.clone()]
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    e2e_steps = max(2, args.steps)   # as long as the device-timed run, so both see the same power state
+    ev_in = [torch.cuda.Event() for _ in range(e2e_steps)]
+    ev_done = [torch.cuda.Event() for _ in range(e2e_steps)]
+    ev_out = [torch.cuda.Event() for _ in range(e2e_steps)]
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_steps = max(1, min(args.steps, 10))
     e0.record(stream)
-    for _ in range(e2e_steps):
-        x.copy_(xh, non_blocking=True)
-        mod.copy_(modh, non_blocking=True)
-        pos.copy_(posh, non_blocking=True)
-        step()
-        xo.copy_(x, non_blocking=True)
+    up.wait_event(e0)
+    down.wait_event(e0)
+    for i in range(e2e_steps):
+        k = i % 2
+        with torch.cuda.stream(up):
+            if i >= 2:
+                up.wait_event(ev_out[i - 2])     # buffer k's previous result has been read back
+            xb[k].copy_(xh, non_blocking=True)
+            mb[k].copy_(modh, non_blocking=True)
+            pb[k].copy_(posh, non_blocking=True)
+            ev_in[i].record(up)
+        stream.wait_event(ev_in[i])
+        H.h3dit_block_forward(shape, bw, mb[k], xb[k], pb[k], n, wsb, nbytes, stream)
+        ev_done[i].record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(ev_done[i])
+            xo[k].copy_(xb[k], non_blocking=True)
+            ev_out[i].record(down)
+    stream.wait_event(ev_out[e2e_steps - 1])
     e1.record(stream)
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1)) / e2e_steps
     h2d = xh.numel() * 2 + modh.numel() * 4 + posh.numel() * 4
-    d2h = xo.numel() * 2
+    d2h = xo[0].numel() * 2
 
     del wsb
     # ---- the same block on the dynamic-int8 path
@@ -429,7 +459,8 @@ def run_ours(args):
                        "l2": "inputs larger than L2: 629 MB of block weights streamed every step"},
             "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu,
             "e2e": {"value": ranks.throughput(fl, e2e_ms) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "pipelining": "uploads and downloads on their own streams, device buffers double-buffered"},
             "gpu_launches": int(launches), "clocks": clocks, "int8": int8_res, "final_layer": final_res,
             "step": step_res,
         }
@@ -496,13 +527,13 @@ def run_int8_block(args, H, synth, torch, stream, barrier, max_over_ranks, rank,
         del q8
     names = ("w_qkv", "w_o", "w1", "w2")
     variants = (("int8", H.INT8, names), ("int8_mlp", H.INT8_MLP, ("w1", "w2")), ("int8_qkv", H.INT8_QKV, ("w_qkv",)))
-    burst, _, _, peak_src = measured_peaks()
+    burst, sustained, _, peak_src = measured_peaks()
     gops = gemm_flops(n, d, f)
     res = {"workload": "block_512_int8: the block_512 shapes with int8 QKV/out-proj/FC1/FC2 (per-token activation "
                        "scales, per-output-channel weight scales, FC2 one scale per 1024 input channels), BF16 attention; "
                        "variants with the MLP alone and QKV alone in int8",
            "peak_note": f"int8 codes run exactly on the BF16 tensor path (sm_103a has no integer tcgen05 MMA): "
-                        f"peak = {peak_src} bf16 burst {burst}"}
+                        f"peaks = {peak_src} bf16 sustained {sustained} / burst {burst}"}
     for name, prec, q_names in variants:
         shape = H.BlockShape(w.d, w.heads, w.head_dim, w.ffn, w.eps, w.sections, w.theta, prec)
         ptr = [codes[k] if k in q_names else wdev[k] for k in names]
@@ -537,6 +568,7 @@ def run_int8_block(args, H, synth, torch, stream, barrier, max_over_ranks, rank,
         gemm_ms = sum(cls[k][0] for k in ("qkv", "out_proj", "fc1", "fc2")) / steps
         res[name] = {"ms": ms, "tops": block_flops(n, d, f) / (ms * 1e-3) / 1e12,
                      "gemm_ms": gemm_ms, "gemm_tops": gops / (gemm_ms * 1e-3) / 1e12,
+                     "gemm_frac_of_bf16_sustained": gops / (gemm_ms * 1e-3) / 1e12 / sustained,
                      "gemm_frac_of_bf16_burst": gops / (gemm_ms * 1e-3) / 1e12 / burst,
                      "quant_ms": cls["quant"][0] / steps, "rows_ms": cls["rows"][0] / steps,
                      "attention_ms": cls["attention"][0] / steps, "steps": steps}
