@@ -67,15 +67,47 @@ __device__ __forceinline__ int seg_offset(const SegMap& m, int row) {
   return k * m.stride;
 }
 
+// A thread's part of a row: NV vectors of 8 values, held either as fp32 or
+// as packed BF16 pairs (exact when every value is a BF16 number; half the
+// registers).
+template <int NV, bool PACKED>
+struct RowRegs;
+template <int NV>
+struct RowRegs<NV, true> {
+  uint4 p[NV];
+  __device__ __forceinline__ void get(int i, float (&v)[8]) const { unpack8(p[i], v); }
+  __device__ __forceinline__ void set(int i, const float (&v)[8]) { p[i] = pack8(v); }
+  __device__ __forceinline__ void set_packed(int i, uint4 u) { p[i] = u; }
+};
+template <int NV>
+struct RowRegs<NV, false> {
+  float f[NV][8];
+  __device__ __forceinline__ void get(int i, float (&v)[8]) const {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = f[i][e];
+  }
+  __device__ __forceinline__ void set(int i, const float (&v)[8]) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[i][e] = v[e];
+  }
+  __device__ __forceinline__ void set_packed(int i, uint4 u) { unpack8(u, f[i]); }
+};
+
 // NV = ceil(d / (8 * 128)) 16-byte vectors per thread: the row's register
 // copy is sized to the actual width.  The kernel is latency-bound on its two
-// block reductions, so resident rows per SM set its bandwidth: up to NV = 5
-// (d <= 5120) the registers are capped for 8 CTAs per SM.
-template <int NV>
-constexpr int row_min_blocks() { return NV <= 5 ? 8 : 5; }
+// block reductions, so resident rows per SM set its bandwidth: with the row
+// held as packed BF16 pairs, up to NV = 5 (d <= 5120) the registers are
+// capped for 10 CTAs per SM.  The gated residual + AdaLN (no quantisation)
+// keeps its row in fp32 at 8 CTAs per SM: its gate and branch values need
+// the registers and the unpacking costs it more than the residency gains
+// (measured at d = 5120).
+template <bool GATE, bool NORM, bool QUANT>
+__host__ __device__ constexpr bool row_packed() { return !(GATE && NORM && !QUANT); }
+template <bool GATE, bool NORM, bool QUANT, int NV>
+constexpr int row_min_blocks() { return NV > 5 ? 8 : row_packed<GATE, NORM, QUANT>() ? 10 : 8; }
 
 template <bool GATE, bool NORM, bool QUANT, int NV>
-__global__ void __launch_bounds__(kRowThreads, row_min_blocks<NV>())
+__global__ void __launch_bounds__(kRowThreads, row_min_blocks<GATE, NORM, QUANT, NV>())
     gate_adaln_kernel(__nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ branch,
                       const float* __restrict__ gate, const float* __restrict__ shift,
                       const float* __restrict__ scale, __nv_bfloat16* __restrict__ h,
@@ -93,13 +125,17 @@ __global__ void __launch_bounds__(kRowThreads, row_min_blocks<NV>())
   const int nvec = d >> 3;
   uint4* xr = reinterpret_cast<uint4*>(x + row * d);
   const uint4* br = reinterpret_cast<const uint4*>(branch + (GATE ? row * d : 0));
-  float v[NV][8];
+  // Every value of the row is exactly a BF16 number (the input, or the
+  // residual after its BF16 rounding), so packing it loses nothing.
+  RowRegs<NV, row_packed<GATE, NORM, QUANT>()> pv;
   float sum = 0.f;
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     const int idx = i * kRowThreads + threadIdx.x;
     if (idx < nvec) {
-      unpack8(xr[idx], v[i]);
+      float v[8];
+      pv.set_packed(i, xr[idx]);
+      pv.get(i, v);
       if (GATE) {
         float b[8];
         unpack8(br[idx], b);
@@ -107,13 +143,14 @@ __global__ void __launch_bounds__(kRowThreads, row_min_blocks<NV>())
         const float4 g1 = __ldg(reinterpret_cast<const float4*>(gate) + 2 * idx + 1);
         const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[i][e] = fmaf(g[e], b[e], v[i][e]);
-        const uint4 packed = pack8(v[i]);
+        for (int e = 0; e < 8; ++e) v[e] = fmaf(g[e], b[e], v[e]);
+        const uint4 packed = pack8(v);
         xr[idx] = packed;
-        unpack8(packed, v[i]);   // continue with the rounded residual
+        pv.set_packed(i, packed);
+        pv.get(i, v);   // continue with the rounded residual
       }
 #pragma unroll
-      for (int e = 0; e < 8; ++e) sum += v[i][e];
+      for (int e = 0; e < 8; ++e) sum += v[e];
     }
   }
   if (!NORM) return;
@@ -123,9 +160,11 @@ __global__ void __launch_bounds__(kRowThreads, row_min_blocks<NV>())
   for (int i = 0; i < NV; ++i) {
     const int idx = i * kRowThreads + threadIdx.x;
     if (idx < nvec) {
+      float v[8];
+      pv.get(i, v);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float t = v[i][e] - mean;
+        const float t = v[e] - mean;
         sq = fmaf(t, t, sq);
       }
     }
@@ -137,6 +176,8 @@ __global__ void __launch_bounds__(kRowThreads, row_min_blocks<NV>())
   for (int i = 0; i < NV; ++i) {
     const int idx = i * kRowThreads + threadIdx.x;
     if (idx < nvec) {
+      float v[8];
+      pv.get(i, v);
       const float4 s0 = __ldg(reinterpret_cast<const float4*>(scale) + 2 * idx);
       const float4 s1 = __ldg(reinterpret_cast<const float4*>(scale) + 2 * idx + 1);
       const float4 b0 = __ldg(reinterpret_cast<const float4*>(shift) + 2 * idx);
@@ -145,9 +186,9 @@ __global__ void __launch_bounds__(kRowThreads, row_min_blocks<NV>())
       const float sh[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
       float o[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = fmaf((v[i][e] - mean) * rstd, 1.f + sc[e], sh[e]);
+      for (int e = 0; e < 8; ++e) o[e] = fmaf((v[e] - mean) * rstd, 1.f + sc[e], sh[e]);
       if (QUANT) {
-        unpack8(pack8(o), v[i]);   // keep bf16(h) for the codes below
+        pv.set_packed(i, pack8(o));   // keep bf16(h) for the codes below
       } else {
         hr[idx] = pack8(o);
       }
@@ -159,8 +200,10 @@ __global__ void __launch_bounds__(kRowThreads, row_min_blocks<NV>())
   for (int i = 0; i < NV; ++i) {
     const int idx = i * kRowThreads + threadIdx.x;
     if (idx < nvec) {
+      float v[8];
+      pv.get(i, v);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[i][e]));
+      for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[e]));
     }
   }
 #pragma unroll
@@ -175,9 +218,11 @@ __global__ void __launch_bounds__(kRowThreads, row_min_blocks<NV>())
   for (int i = 0; i < NV; ++i) {
     const int idx = i * kRowThreads + threadIdx.x;
     if (idx < nvec) {
+      float v[8];
+      pv.get(i, v);
       float c[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) c[e] = static_cast<float>(quant_code(v[i][e], sq8));
+      for (int e = 0; e < 8; ++e) c[e] = static_cast<float>(quant_code(v[e], sq8));
       hr[idx] = pack8(c);   // integers in [-127, 127]: exact in BF16
     }
   }
