@@ -382,6 +382,9 @@ def run_ours(args):
         kernels["row_kernels"]["bytes_per_block"] = rows_bytes
         kernels["row_kernels"]["gbs"] = rows_gbs
         kernels["row_kernels"]["frac_of_hbm"] = rows_gbs / hbm
+        kernels["row_kernels"]["timing"] = ("CUDA events around each launch inside the block loop, at the "
+                                            "power-capped SM clock of the run (the row kernels' two block "
+                                            "reductions make them slower at lower SM clocks)")
 
     # The timed region is 200+ back-to-back blocks with the power cap engaged
     # (see clocks), i.e. kernels inside a long step: the denominator is the
