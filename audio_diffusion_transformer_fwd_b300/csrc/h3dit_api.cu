@@ -213,7 +213,23 @@ h3::PairGrid pair_grid(const h3dit_video_grid* g, int n_tokens) {
 // ------------------------------------------------------------------ launches
 template <typename K>
 h3dit_status set_smem(K kernel, size_t bytes) {
+  // Dynamic shared memory above 48 KB is opted into per kernel and per
+  // device: once per (kernel, device) pair, whatever thread gets there first.
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, uint64_t>> done;   // kernel -> bit per device ordinal
+  int dev = 0;
+  H3_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(H3DIT_E_UNSUPPORTED, "device ordinal %d out of range", dev);
+  const void* key = reinterpret_cast<const void*>(kernel);
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = std::find_if(done.begin(), done.end(), [&](const std::pair<const void*, uint64_t>& e) {
+    return e.first == key;
+  });
+  if (it != done.end() && (it->second >> dev & 1u)) return H3DIT_OK;
   H3_CUDA(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes));
+  if (it == done.end()) done.emplace_back(key, 0);
+  for (auto& e : done)
+    if (e.first == key) e.second |= uint64_t(1) << dev;
   return H3DIT_OK;
 }
 
@@ -253,20 +269,17 @@ h3dit_status launch_gemm(int epi, const void* A, const void* B, int M, int N, in
   TimedLaunch tl(cls, s);
   switch (epi) {
     case h3::kEpiStore: {
-      static bool once = false;
-      if (!once) { H3_TRY(set_smem(h3::gemm_bf16_tc_kernel<h3::kEpiStore>, h3::kGemmSmemBytes)); once = true; }
+      H3_TRY(set_smem(h3::gemm_bf16_tc_kernel<h3::kEpiStore>, h3::kGemmSmemBytes));
       h3::gemm_bf16_tc_kernel<h3::kEpiStore><<<grid, h3::kGemmThreads, h3::kGemmSmemBytes, s>>>(ta, tb, args);
       break;
     }
     case h3::kEpiGelu: {
-      static bool once = false;
-      if (!once) { H3_TRY(set_smem(h3::gemm_bf16_tc_kernel<h3::kEpiGelu>, h3::kGemmSmemBytes)); once = true; }
+      H3_TRY(set_smem(h3::gemm_bf16_tc_kernel<h3::kEpiGelu>, h3::kGemmSmemBytes));
       h3::gemm_bf16_tc_kernel<h3::kEpiGelu><<<grid, h3::kGemmThreads, h3::kGemmSmemBytes, s>>>(ta, tb, args);
       break;
     }
     case h3::kEpiQKV: {
-      static bool once = false;
-      if (!once) { H3_TRY(set_smem(h3::gemm_bf16_tc_kernel<h3::kEpiQKV>, h3::kGemmSmemBytes)); once = true; }
+      H3_TRY(set_smem(h3::gemm_bf16_tc_kernel<h3::kEpiQKV>, h3::kGemmSmemBytes));
       h3::gemm_bf16_tc_kernel<h3::kEpiQKV><<<grid, h3::kGemmThreads, h3::kGemmSmemBytes, s>>>(ta, tb, args);
       break;
     }
@@ -280,11 +293,7 @@ h3dit_status launch_gemm(int epi, const void* A, const void* B, int M, int N, in
 template <int EPI, int MODE>
 h3dit_status launch_i8_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const h3::GemmArgs& args,
                               const h3::I8Args& qa, int grid, cudaStream_t s) {
-  static bool once = false;
-  if (!once) {
-    H3_TRY(set_smem(h3::gemm_i8x_tc_kernel<EPI, MODE>, h3::kGemmSmemBytes));
-    once = true;
-  }
+  H3_TRY(set_smem(h3::gemm_i8x_tc_kernel<EPI, MODE>, h3::kGemmSmemBytes));
   h3::gemm_i8x_tc_kernel<EPI, MODE><<<grid, h3::kI8Threads, h3::kGemmSmemBytes, s>>>(ta, tb, args, qa);
   H3_CUDA(cudaGetLastError());
   return H3DIT_OK;
@@ -363,12 +372,10 @@ h3dit_status launch_attention(const h3dit_config* c, const void* q, const void* 
   dim3 grid((n + rows_per_cta - 1) / rows_per_cta, H);
   TimedLaunch tl(kAttn, s);
   if (dh == 128) {
-    static bool once = false;
-    if (!once) { H3_TRY(set_smem(h3::attn_fwd_tc_kernel<128>, h3::AttnSmem<128>::kTotal)); once = true; }
+    H3_TRY(set_smem(h3::attn_fwd_tc_kernel<128>, h3::AttnSmem<128>::kTotal));
     h3::attn_fwd_tc_kernel<128><<<grid, h3::kAttnThreads, h3::AttnSmem<128>::kTotal, s>>>(tq, tk, tv, a);
   } else {
-    static bool once = false;
-    if (!once) { H3_TRY(set_smem(h3::attn_fwd_tc_kernel<64>, h3::AttnSmem<64>::kTotal)); once = true; }
+    H3_TRY(set_smem(h3::attn_fwd_tc_kernel<64>, h3::AttnSmem<64>::kTotal));
     h3::attn_fwd_tc_kernel<64><<<grid, h3::kAttnThreads, h3::AttnSmem<64>::kTotal, s>>>(tq, tk, tv, a);
   }
   H3_CUDA(cudaGetLastError());
@@ -1036,11 +1043,7 @@ h3dit_status h3dit_final_layer(const h3dit_config* cfg, const void* x, int n_tok
     if (!aligned(h.w, 16) || !aligned(h.out, 16) || !aligned(h.shift, 16) || !aligned(h.scale, 16))
       return fail(H3DIT_E_INVAL, "head %d tensors must be 16-byte aligned", i);
   }
-  static bool once = false;
-  if (!once) {
-    H3_TRY(set_smem(h3::final_head_kernel, h3::kHeadSmemLimit + 1536));
-    once = true;
-  }
+  H3_TRY(set_smem(h3::final_head_kernel, h3::kHeadSmemLimit + 1536));
   h3::HeadBatch hb{};
   {
     const uint64_t dims[2] = {(uint64_t)d, (uint64_t)n_tokens};

@@ -207,3 +207,37 @@ def test_core_reuse_replays_a_step():
     # x + delta in fp32 then BF16 versus the exact sum rounded once: equal
     # except where the fp32 sum lands on a BF16 rounding tie (double rounding)
     assert np.mean(got != ref) < 1e-3 and max_abs(got, ref) <= 2.0 ** -7 * float(np.max(np.abs(ref)))
+
+
+def test_step_replays_from_a_cuda_graph():
+    """The step is stream-ordered and allocation-free, so a CUDA graph
+    captured around h3dit_step_forward replays it bit for bit (eager calls
+    first, which set up the kernels' shared-memory attributes)."""
+    w = TINY
+    n = w.n_tokens
+    shape = shape_of(w)
+    pos = dev_f32(synth.positions(w.video, w.n_text, w.n_audio))
+    x = synth.host_activations(n, w.d, seed=61)
+    nb = 3
+    devs = [_weights_dev(synth.host_block_weights(w.d, w.ffn, seed=61, block=b)) for b in range(nb)]
+    mods = dev_f32(np.stack([synth.host_mod(w.d, seed=61, block=b) for b in range(nb)]))
+    T, Hh, W = w.video
+    tr = H.reduction(H.video_grid(0, T, Hh, W), 0, 2)
+    nbytes = H.h3dit_workspace_size(shape, n, tr)
+    ws = torch.empty(nbytes, device="cuda", dtype=torch.uint8)
+    bws = [dv[1] for dv in devs]
+    eager = dev_bf16(x)
+    H.h3dit_step_forward(shape, bws, mods, eager, pos, n, tr, ws, nbytes)
+    H.h3dit_check_device_error()
+    xg = dev_bf16(x)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        H.h3dit_step_forward(shape, bws, mods, xg, pos, n, tr, ws, nbytes, s)
+    for _ in range(2):
+        xg.copy_(dev_bf16(x))
+        graph.replay()
+        torch.cuda.synchronize()
+        H.h3dit_check_device_error()
+        assert torch.equal(xg, eager)

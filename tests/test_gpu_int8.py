@@ -375,3 +375,31 @@ def test_int8_variant_step_equals_blocks(prec):
         H.h3dit_block_forward(shape, packs[b][1], dev_f32(mods[b]), xb, dev_f32(pos), n, ws, nbytes)
     H.h3dit_check_device_error()
     assert torch.equal(xs, xb)
+
+
+def test_int8_step_with_token_reduction():
+    """The int8 step through a token reduction: the reduced blocks' AdaLN
+    codes come from the reduced stream, and the result follows the oracle's
+    int8 step."""
+    w = TINY
+    n = w.n_tokens
+    shape = shape_of(w, H.INT8)
+    pos = synth.positions(w.video, w.n_text, w.n_audio)
+    x = synth.host_activations(n, w.d, seed=71)
+    nb = 3
+    wts = [synth.host_block_weights(w.d, w.ffn, seed=71, block=b) for b in range(nb)]
+    packs = [_int8_weights(t) for t in wts]
+    mods = np.stack([synth.host_mod(w.d, seed=71, block=b) for b in range(nb)])
+    T, Hh, W = w.video
+    tr = H.reduction(H.video_grid(0, T, Hh, W), 0, 2)
+    nbytes = H.h3dit_workspace_size(shape, n, tr)
+    ws = torch.empty(nbytes, device="cuda", dtype=torch.uint8)
+    xd = dev_bf16(x)
+    H.h3dit_step_forward(shape, [p[2] for p in packs], dev_f32(mods), xd, dev_f32(pos), n, tr, ws, nbytes)
+    H.h3dit_check_device_error()
+    got = host(xd)
+    red = O.Reduction(O.VideoGrid(0, T, Hh, W), 0, 2)
+    cfg = oracle_cfg(w)
+    ref_bf = O.step_forward(x, [p[0] for p in packs], list(mods), pos, cfg, reduction=red, bf16_storage=True,
+                            int8=True)
+    assert rel_l2(got, ref_bf) <= 1e-2 * nb and rel_l2(got - x, ref_bf - x) <= 2e-2 * nb

@@ -155,3 +155,30 @@ def test_malformed_segments_refused():
     with pytest.raises(H.H3DitError) as e:
         H.h3dit_step_forward_seg(shape, [bw], mods, H.segments([0, 100]), xd, pos, n, tr, ws, nbytes)
     assert e.value.status == H.E_INVAL and "inside" in H.lib().h3dit_last_error().decode()
+
+
+def test_int8_reduced_step_with_segments():
+    from tests.test_gpu_int8 import _int8_weights
+    w = TINY
+    n = w.n_tokens
+    shape = shape_of(w, H.INT8)
+    pos = synth.positions(w.video, w.n_text, w.n_audio)
+    x = synth.host_activations(n, w.d, seed=36)
+    nb = 3
+    wts = [synth.host_block_weights(w.d, w.ffn, seed=36, block=b) for b in range(nb)]
+    packs = [_int8_weights(t) for t in wts]
+    mods = np.stack([_seg_mods(36 + 10 * b) for b in range(nb)])
+    T, Hh, W = w.video
+    tr = H.reduction(H.video_grid(0, T, Hh, W), 0, 2)
+    nbytes = H.h3dit_workspace_size(shape, n, tr)
+    ws = torch.empty(nbytes, device="cuda", dtype=torch.uint8)
+    xd = dev_bf16(x)
+    H.h3dit_step_forward_seg(shape, [p[2] for p in packs], dev_f32(mods), H.segments(STARTS), xd, dev_f32(pos), n,
+                             tr, ws, nbytes)
+    H.h3dit_check_device_error()
+    got = host(xd)
+    cfg = oracle_cfg(w)
+    per_row = [O.segment_mod(mods[b], STARTS, n) for b in range(nb)]
+    red = O.Reduction(O.VideoGrid(0, T, Hh, W), 0, 2)
+    ref_bf = O.step_forward(x, [p[0] for p in packs], per_row, pos, cfg, reduction=red, bf16_storage=True, int8=True)
+    assert rel_l2(got, ref_bf) <= 1e-2 * nb and rel_l2(got - x, ref_bf - x) <= 2e-2 * nb
