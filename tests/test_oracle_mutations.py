@@ -48,6 +48,25 @@ MUTATIONS = [
     ("reduced_token_count", "grid.T * grid.Hh *", "grid.Hh *", [P.test_token_counts_of_the_workloads, P.test_reduce_restore_identity_and_pairs]),
     ("step_forward", "b == reduction.restore_before_block", "b == reduction.restore_before_block + 1", [P.test_step_with_reduction_boundaries]),
     ("step_forward", "b == reduction.reduce_after_block", "b == reduction.reduce_after_block + 1", [P.test_step_with_reduction_boundaries]),
+    # int8 projection selection
+    ("block_forward_int8", 'if "qkv" in which:', 'if "o" in which:', [P.test_int8_block_without_int8_projections_is_the_float_block]),
+    ("block_forward_int8", 'fc2_int8(uq, us, w["q2"], w["s2"], g2)', 'fc2_int8(uq, us, w["q2"], w["s1"][:w["q2"].shape[0]], g2)',
+     [P.test_int8_block_close_to_float_block, P.test_int8_block_without_int8_projections_is_the_float_block]),
+    # per-segment modulation
+    ("segment_mod", "seg[starts[s_]:starts[s_ + 1]] = s_", "seg[starts[s_]:starts[s_ + 1]] = min(s_, 1)",
+     [P.test_segment_mod_equals_per_segment_blocks]),
+    ("_mod_parts", "(v[sel] for v in (gate1, shift2, scale2, gate2))", "(v[sel] for v in (gate1, scale2, shift2, gate2))",
+     [P.test_segment_mod_equals_per_segment_blocks]),
+    ("_reduce_mod_rows", "return mod[:, first, :]", "return mod[:, :len(first), :]", [P.test_step_reduction_with_segments]),
+    # final layer
+    ("final_head", "adaln(xs, np.asarray(shift, np.float64), np.asarray(scale, np.float64), eps)",
+     "adaln(xs, np.asarray(scale, np.float64), np.asarray(shift, np.float64), eps)", [P.test_final_head_scalar_loops]),
+    ("final_head", "[row_start:row_start + rows]", "[row_start + 1:row_start + rows + 1]", [P.test_final_head_scalar_loops]),
+    # core residual reuse
+    ("core_reuse", "np.asarray(x, np.float64) + np.asarray(delta, np.float64)",
+     "np.asarray(x, np.float64) - np.asarray(delta, np.float64)", [P.test_core_reuse_replays_the_core_exactly]),
+    ("core_residual", "np.asarray(x_out, np.float64) - np.asarray(x_in, np.float64)",
+     "np.asarray(x_in, np.float64) - np.asarray(x_out, np.float64)", [P.test_core_reuse_replays_the_core_exactly]),
 ]
 
 
