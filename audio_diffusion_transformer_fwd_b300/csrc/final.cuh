@@ -5,26 +5,30 @@
 // tiles are loaded, so no normalised copy of the rows is ever stored:
 //   out[r][c] = bf16( sum_k bf16(LN(x_r)_k (1 + scale_k) + shift_k) * w[c][k] )
 //
-// Two kernels:
+// Two kernels, each one launch for all heads:
 //  * head_stats_kernel: one warp per row, coalesced passes for the mean and
 //    the centred variance; (mean, rstd) are parked in the first 8 bytes of
 //    the row's own output, which the head kernel reads before it overwrites
 //    the row -- the layer needs no workspace.
-//  * final_head_kernel: one CTA per 128 rows of a head (all heads in one
-//    launch, blockIdx.y = head), 192 threads.  Warp 4
-//    streams raw x tiles (128 rows x 64 columns, 128-byte swizzle), weight
-//    tiles (c_out x 64) and the k-block's scale/shift slices with TMA through
-//    a ring of up to 8 stages; warps 0-3
-//    (one row per thread) normalise and modulate their row's 64 values in
-//    place, in the same swizzled position, and hand the stage to warp 5,
-//    whose elected thread issues tcgen05.mma M128 N c_out K16; at the end
-//    warps 0-3 drain the fp32 accumulator from TMEM.
+//  * final_head_kernel: 128 rows of a head per CTA (blockIdx.y = head), the
+//    d columns split over a cluster of `ksplit` CTAs (one range of k-blocks
+//    each) so that the launch fills the SMs.  320 threads: warp 8 streams
+//    raw x tiles (128 rows x 64 columns, 128-byte swizzle), weight tiles
+//    (c_out x 64) and the k-block's scale/shift slices with TMA through a
+//    ring of up to 8 stages; warps 0-7 (two threads per row, 32 columns
+//    each) normalise and modulate the tile in place, in the same swizzled
+//    position, and hand the stage to warp 9, whose elected thread issues
+//    tcgen05.mma M128 N c_out K16 into TMEM.  At the end each CTA but the
+//    cluster's first parks its fp32 partial sums in its own shared memory;
+//    the first CTA adds them (distributed shared memory), rounds to BF16 and
+//    stores the rows.
 #pragma once
 #include "ptx.cuh"
 
 namespace h3 {
 
-constexpr int kHeadThreads = 192;
+constexpr int kHeadThreads = 320;           // warps 0-7 transform, 8 TMA, 9 MMA
+constexpr int kHeadMaxSplit = 4;           // CTAs per cluster splitting d
 constexpr int kHeadMaxStages = 8;
 constexpr int kHeadBK = 64;
 constexpr int kHeadXBytes = 128 * kHeadBK * 2;   // 16 KB raw x tile, transformed in place
@@ -66,16 +70,31 @@ struct HeadBatch {
   CUtensorMap tmX;                // the residual stream [n][d]
   CUtensorMap tmW[kMaxHeads];     // each head's weight [c_out][d]
   HeadArgs a[kMaxHeads];
+  int ksplit;                     // cluster size along blockIdx.x (1..kHeadMaxSplit)
 };
 
-// (mean, rstd) of rows row_start .. row_start + rows - 1 of x, one warp per
-// row, stored as two floats at the start of out's row.
+// The rows of every head for the statistics pass (one launch).
+struct HeadRows {
+  int n_heads;
+  int first_warp[kMaxHeads + 1];  // prefix sums of the heads' row counts
+  int row_start[kMaxHeads];
+  int c_out[kMaxHeads];
+  __nv_bfloat16* out[kMaxHeads];
+};
+
+// (mean, rstd) of every head row of x, one warp per row, stored as two
+// floats at the start of the row's output.
 __global__ void __launch_bounds__(256)
-    head_stats_kernel(const __nv_bfloat16* __restrict__ x, int row_start, int rows, int d, float eps,
-                      __nv_bfloat16* out, int c_out) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    head_stats_kernel(const __nv_bfloat16* __restrict__ x, const __grid_constant__ HeadRows hr, int d, float eps) {
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (warp >= rows) return;
+  if (gw >= hr.first_warp[hr.n_heads]) return;
+  int h = 0;
+  while (gw >= hr.first_warp[h + 1]) ++h;
+  const int warp = gw - hr.first_warp[h];
+  const int row_start = hr.row_start[h];
+  const int c_out = hr.c_out[h];
+  __nv_bfloat16* out = hr.out[h];
   const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(row_start + warp) * d);
   const int nvec = d >> 3;
   float sum = 0.f;
@@ -116,7 +135,11 @@ __global__ void __launch_bounds__(kHeadThreads, 1) final_head_kernel(const __gri
   const HeadArgs& a = hb.a[blockIdx.y];
   const CUtensorMap* tmX = &hb.tmX;
   const CUtensorMap* tmW = &hb.tmW[blockIdx.y];
-  if (static_cast<int>(blockIdx.x) * 128 >= a.rows) return;   // this head has fewer tiles
+  const int ksplit = hb.ksplit;
+  const int tile0 = (blockIdx.x / ksplit) * 128;
+  // a head with fewer tiles: the whole cluster (same tile) leaves together
+  if (tile0 >= a.rows) return;
+  const int ks = static_cast<int>(blockIdx.x % ksplit);   // == rank in the cluster
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t stage_bytes = head_stage_bytes(a.c_out);
@@ -133,13 +156,13 @@ __global__ void __launch_bounds__(kHeadThreads, 1) final_head_kernel(const __gri
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int tile0 = blockIdx.x * 128;
   const int kblocks = a.d / kHeadBK;
+  const int kb0 = ks * kblocks / ksplit, kb1 = (ks + 1) * kblocks / ksplit;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(ready0 + 8 * s, 128);
+      mbar_init(ready0 + 8 * s, 256);
       mbar_init(empty0 + 8 * s, 1);
     }
     mbar_init(acc_full, 1);
@@ -147,7 +170,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1) final_head_kernel(const __gri
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_holder), a.tmem_cols);
     tmem_relinquish();
   }
@@ -156,11 +179,15 @@ __global__ void __launch_bounds__(kHeadThreads, 1) final_head_kernel(const __gri
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
-  if (warp < 4) {
-    // ---------------- in-place AdaLN of the x tiles, then the epilogue
-    const int r = warp * 32 + lane;
-    const int grow = tile0 + r;
-    const bool live = grow < a.rows;
+  // transform warps: rows (warp & 3) * 32 + lane, column half warp >> 2
+  const int r = (warp & 3) * 32 + lane;
+  const int hh = (warp >> 2) & 1;
+  const int grow = tile0 + r;
+  const bool live = grow < a.rows;
+  bool ok = true;
+
+  if (warp < 8) {
+    // ---------------- in-place AdaLN of the x tiles
     float mean = 0.f, rstd = 0.f;
     if (live) {
       const float2 st = *reinterpret_cast<const float2*>(a.out + static_cast<size_t>(grow) * a.c_out);
@@ -170,23 +197,26 @@ __global__ void __launch_bounds__(kHeadThreads, 1) final_head_kernel(const __gri
     const uint32_t mod_off = head_mod_offset(a.c_out);
     int stage = 0;
     uint32_t phase = 0;
-    bool ok = true;
-    for (int kb = 0; kb < kblocks; ++kb) {
+    for (int kb = kb0; kb < kb1; ++kb) {
       if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) { ok = false; break; }
       uint8_t* st_base = smem + stage * stage_bytes;
       uint8_t* row = st_base + r * 128;
       const float4* sc4 = reinterpret_cast<const float4*>(st_base + mod_off);            // 64 scales
       const float4* sh4 = reinterpret_cast<const float4*>(st_base + mod_off + kHeadBK * 4);   // 64 shifts
-      // all eight 16-byte chunks of the row first, then the writes: the
-      // loads are not ordered behind earlier stores to the same tile
-      uint4 raw[8];
+      // this thread's four 16-byte chunks of the row first, then the writes:
+      // the loads are not ordered behind earlier stores to the same tile
+      uint4 raw[4];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) raw[c] = *reinterpret_cast<const uint4*>(row + ((c ^ (r & 7)) * 16));   // 128-byte swizzle
+      for (int q = 0; q < 4; ++q) {
+        const int c = hh * 4 + q;
+        raw[q] = *reinterpret_cast<const uint4*>(row + ((c ^ (r & 7)) * 16));   // 128-byte swizzle
+      }
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int q = 0; q < 4; ++q) {
+        const int c = hh * 4 + q;
         uint4 packed = make_uint4(0u, 0u, 0u, 0u);
         if (live) {
-          const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw[c]);
+          const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw[q]);
           const float4 s0 = sc4[2 * c], s1 = sc4[2 * c + 1];
           const float4 h0 = sh4[2 * c], h1 = sh4[2 * c + 1];
           const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
@@ -208,24 +238,9 @@ __global__ void __launch_bounds__(kHeadThreads, 1) final_head_kernel(const __gri
       mbar_arrive(ready0 + 8 * stage);
       if (++stage == S) { stage = 0; phase ^= 1; }
     }
-    if (ok && mbar_wait(acc_full, 0, abort_flag)) {
-      tc_fence_after();
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(warp * 32) << 16);
-#pragma unroll 1
-      for (int cg = 0; cg < a.c_out / 16; ++cg) {
-        float v[16];
-        tmem_ld16(tbase + cg * 16, v);
-        if (live) {
-          uint32_t p[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) p[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-          uint4* o = reinterpret_cast<uint4*>(a.out + static_cast<size_t>(grow) * a.c_out + cg * 16);
-          o[0] = make_uint4(p[0], p[1], p[2], p[3]);
-          o[1] = make_uint4(p[4], p[5], p[6], p[7]);
-        }
-      }
-    }
-  } else if (warp == 4) {
+    ok = ok && mbar_wait(acc_full, 0, abort_flag);
+    if (ok) tc_fence_after();
+  } else if (warp == 8) {
     if (lane == 0) {
       // ---------------- raw x tiles and weight tiles by TMA
       tma_prefetch_desc(tmX);
@@ -233,7 +248,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1) final_head_kernel(const __gri
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
-      for (int kb = 0; kb < kblocks; ++kb) {
+      for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) break;
         const uint32_t fb = full0 + 8 * stage;
         const uint32_t base = smem_u32(smem + stage * stage_bytes);
@@ -246,9 +261,9 @@ __global__ void __launch_bounds__(kHeadThreads, 1) final_head_kernel(const __gri
         ++issued;
         if (++stage == S) { stage = 0; phase ^= 1; }
       }
-      if (issued < kblocks) {
+      if (issued < kb1 - kb0) {
         // after a timeout: let the loads in flight land before exiting
-        for (int kb = max(0, issued - S); kb < issued; ++kb) mbar_wait_drain(full0 + 8 * (kb % S), (kb / S) & 1);
+        for (int i = max(0, issued - S); i < issued; ++i) mbar_wait_drain(full0 + 8 * (i % S), (i / S) & 1);
       }
     }
   } else {
@@ -257,28 +272,80 @@ __global__ void __launch_bounds__(kHeadThreads, 1) final_head_kernel(const __gri
       const uint32_t idesc = idesc_bf16_f32(128, a.c_out);
       int stage = 0;
       uint32_t phase = 0;
-      bool ok = true;
-      for (int kb = 0; kb < kblocks; ++kb) {
-        if (!mbar_wait(ready0 + 8 * stage, phase, abort_flag)) { ok = false; break; }
+      bool mok = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(ready0 + 8 * stage, phase, abort_flag)) { mok = false; break; }
         tc_fence_after();
         const uint32_t a0 = smem_u32(smem + stage * stage_bytes);
         const uint32_t b0 = a0 + kHeadXBytes;
 #pragma unroll
         for (int k = 0; k < kHeadBK / 16; ++k)
-          tc_mma_bf16(tmem_base, sdesc_k128(a0 + 32 * k), sdesc_k128(b0 + 32 * k), idesc, (kb | k) != 0);
+          tc_mma_bf16(tmem_base, sdesc_k128(a0 + 32 * k), sdesc_k128(b0 + 32 * k), idesc, (kb != kb0 || k != 0));
         tc_commit(empty0 + 8 * stage);
         if (++stage == S) { stage = 0; phase ^= 1; }
       }
-      if (ok) tc_commit(acc_full);
+      if (mok) tc_commit(acc_full);
       tc_commit(drain);
       mbar_wait_drain(drain, 0);
     }
   }
 
+  // ---------------- epilogue: warps w and w + 4 share TMEM lanes 32 (w & 3)
+  // and take alternate halves of the 16-column groups.  All stage buffers
+  // are consumed (acc_full), so the partial sums reuse shared memory from 0.
+  const int groups = a.c_out / 16;
+  const int gh = (groups + 1) / 2;
+  const int g0 = hh * gh, g1 = min(groups, g0 + gh);
+  const uint32_t tl = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+  const int pstride = a.c_out + 4;   // floats per partial row (16-byte shift per row)
+  float* part = reinterpret_cast<float*>(smem);
+  if (ksplit > 1) {
+    if (warp < 8 && ok && ks != 0) {
+#pragma unroll 1
+      for (int cg = g0; cg < g1; ++cg) {
+        float v[16];
+        tmem_ld16(tl + cg * 16, v);
+        float4* dst = reinterpret_cast<float4*>(part + r * pstride + cg * 16);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      }
+    }
+    // every thread of every CTA of the cluster, whatever happened above
+    cluster_sync_all();
+  }
+  if (warp < 8 && ok && ks == 0) {
+#pragma unroll 1
+    for (int cg = g0; cg < g1; ++cg) {
+      float v[16];
+      tmem_ld16(tl + cg * 16, v);
+      for (int peer = 1; peer < ksplit; ++peer) {
+        const uint32_t src = mapa_shared(smem_u32(part + r * pstride + cg * 16), static_cast<uint32_t>(peer));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 q = ld_cluster_f4(src + 16 * i);
+          v[4 * i] += q.x;
+          v[4 * i + 1] += q.y;
+          v[4 * i + 2] += q.z;
+          v[4 * i + 3] += q.w;
+        }
+      }
+      if (live) {
+        uint32_t p[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) p[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+        uint4* o = reinterpret_cast<uint4*>(a.out + static_cast<size_t>(grow) * a.c_out + cg * 16);
+        o[0] = make_uint4(p[0], p[1], p[2], p[3]);
+        o[1] = make_uint4(p[4], p[5], p[6], p[7]);
+      }
+    }
+  }
+  // the peers' partial sums stay readable until the first CTA is done
+  if (ksplit > 1) cluster_sync_all();
+
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem_base, a.tmem_cols);
+  if (warp == 9) tmem_dealloc(tmem_base, a.tmem_cols);
 }
 
 }  // namespace h3

@@ -1051,9 +1051,10 @@ h3dit_status h3dit_final_layer(const h3dit_config* cfg, const void* x, int n_tok
     const uint32_t box[2] = {h3::kHeadBK, 128};
     H3_TRY(make_map(&hb.tmX, x, 2, dims, str, box));
   }
-  int max_tiles = 0;
+  int max_tiles = 0, all_tiles = 0;
   size_t smem = 0;
-  TimedLaunch tl(kRows, stream);
+  h3::HeadRows hr{};
+  hr.n_heads = n_heads;
   for (int i = 0; i < n_heads; ++i) {
     const h3dit_final_head& h = heads[i];
     const uint64_t dims[2] = {(uint64_t)d, (uint64_t)h.c_out};
@@ -1073,13 +1074,36 @@ h3dit_status h3dit_final_layer(const h3dit_config* cfg, const void* x, int n_tok
     a.tmem_cols = cols;
     a.stages = h3::head_stages(h.c_out);
     max_tiles = std::max(max_tiles, (h.rows + 127) / 128);
+    all_tiles += (h.rows + 127) / 128;
     smem = std::max(smem, h3::head_smem_bytes(h.c_out));
-    h3::head_stats_kernel<<<(h.rows * 32 + 255) / 256, 256, 0, stream>>>(static_cast<const bf16*>(x), h.row_start,
-                                                                         h.rows, d, cfg->eps, a.out, h.c_out);
-    H3_CUDA(cudaGetLastError());
+    hr.first_warp[i + 1] = hr.first_warp[i] + h.rows;
+    hr.row_start[i] = h.row_start;
+    hr.c_out[i] = h.c_out;
+    hr.out[i] = static_cast<bf16*>(h.out);
   }
-  h3::final_head_kernel<<<dim3(max_tiles, n_heads), h3::kHeadThreads, smem, stream>>>(hb);
+  // split d over a cluster of CTAs so the launch fills the SMs (one wave:
+  // every cluster of a tile must fit at once)
+  int ksplit = std::max(1, std::min(h3::kHeadMaxSplit, sm_count() / all_tiles));
+  ksplit = std::min(ksplit, d / h3::kHeadBK);
+  hb.ksplit = ksplit;
+  TimedLaunch tl(kRows, stream);
+  const long long stat_threads = (long long)hr.first_warp[n_heads] * 32;
+  h3::head_stats_kernel<<<(unsigned)((stat_threads + 255) / 256), 256, 0, stream>>>(static_cast<const bf16*>(x), hr,
+                                                                                    d, cfg->eps);
   H3_CUDA(cudaGetLastError());
+  cudaLaunchConfig_t lc{};
+  lc.gridDim = dim3(max_tiles * ksplit, n_heads);
+  lc.blockDim = dim3(h3::kHeadThreads);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = ksplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = ksplit > 1 ? 1 : 0;
+  H3_CUDA(cudaLaunchKernelEx(&lc, h3::final_head_kernel, hb));
   return H3DIT_OK;
 }
 

@@ -69,6 +69,16 @@ def test_final_layer_ragged_heads(r0, rows, c):
     _check(x, hosts, w.eps)
 
 
+@pytest.mark.parametrize("rows", [5120, 9728])
+def test_final_layer_cluster_splits(rows):
+    """Enough 128-row tiles that the head kernel splits d over 3 CTAs (40
+    tiles, uneven k-block ranges at d = 256) or does not split (76 tiles)."""
+    w = TINY
+    x = synth.host_activations(rows + 8, w.d, seed=45, std=2.0)
+    hosts = _run(w, x, [(5, rows, 64)], seed=45)
+    _check(x, hosts, w.eps)
+
+
 @pytest.mark.slow
 def test_final_layer_512_class_sampled_rows():
     """Video rows 0..6143 and audio rows 6656..6911 of the 512-class stream."""
