@@ -649,6 +649,8 @@ def run_profile(args):
     torch.cuda.set_device(0)
     w = synth.WORKLOADS["block_512"]
     n, d, f = w.n_tokens, w.d, w.ffn
+    if args.profile == "final":
+        return run_profile_final(args, H, synth, torch, w)
     if args.tokens:
         n = max(1, min(n, args.tokens))
     prec = H.INT8 if args.profile == "int8" else H.BF16
@@ -680,6 +682,31 @@ def run_profile(args):
     return 0
 
 
+def run_profile_final(args, H, synth, torch, w):
+    """The final layer of the 512 class (video head rows 0..6143, audio head
+    rows 6656..6911, 64 channels each) run warmup + steps times, no timing:
+    two launches per layer (row statistics, head GEMM)."""
+    n, d = w.n_tokens, w.d
+    shape = H.BlockShape(w.d, w.heads, w.head_dim, w.ffn, w.eps, w.sections, w.theta)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    heads, keep = [], []
+    for r0, rows, c in ((0, 6144, 64), (6656, 256, 64)):
+        sh = torch.randn(d, device="cuda", generator=g) * 0.1
+        sc = torch.randn(d, device="cuda", generator=g) * 0.1
+        wt = (torch.randn((c, d), device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+        out = torch.empty((rows, c), device="cuda", dtype=torch.bfloat16)
+        heads.append(H.final_head(r0, rows, sh, sc, wt, c, out))
+        keep += [sh, sc, wt, out]
+    x = synth.device_activations(n, d, seed=0)
+    for _ in range(args.warmup + args.steps):
+        H.h3dit_final_layer(shape, x, n, heads)
+    H.h3dit_check_device_error()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": "final", "tokens": n, "layers": args.warmup + args.steps}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -690,9 +717,9 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true", help="omit the oracle CPU baseline")
     ap.add_argument("--tokens", type=int, default=None,
                     help="with --profile: run the block on the first TOKENS tokens of the workload (a small case)")
-    ap.add_argument("--profile", choices=["bf16", "int8"], default=None,
-                    help="run only WARMUP + STEPS forwards of the 512-class block (no report): the command "
-                         "the ncu captures under profiles/ run")
+    ap.add_argument("--profile", choices=["bf16", "int8", "final"], default=None,
+                    help="run only WARMUP + STEPS forwards of the 512-class block, or of its final layer "
+                         "(no report): the command the ncu captures under profiles/ run")
     ap.add_argument("--traffic-from", default=None,
                     help="write profiles/ncu_traffic.json from an ncu DRAM-bytes CSV of one block and exit")
     args = ap.parse_args()
