@@ -448,13 +448,31 @@ h3dit_status launch_rows(void* x, const void* branch, const float* gate, const f
   return H3DIT_OK;
 }
 
+// Groups of 256, 512, 768 or 1024 columns: one warp per group (quantize_warp_kernel).
+template <bool CODES>
+bool launch_quantize_warp(const void* x, int rows, int cols, int group, bf16* q16, int8_t* q8, float* scales,
+                          cudaStream_t s) {
+  if (group % 256 != 0 || group > 1024) return false;
+  const long long n_groups = 1LL * rows * (cols / group);
+  const unsigned blocks = (unsigned)((n_groups + 7) / 8);
+  const bf16* xb = static_cast<const bf16*>(x);
+  switch (group / 256) {
+    case 1: h3::quantize_warp_kernel<1, CODES><<<blocks, 256, 0, s>>>(xb, cols, group, n_groups, q16, q8, scales); break;
+    case 2: h3::quantize_warp_kernel<2, CODES><<<blocks, 256, 0, s>>>(xb, cols, group, n_groups, q16, q8, scales); break;
+    case 3: h3::quantize_warp_kernel<3, CODES><<<blocks, 256, 0, s>>>(xb, cols, group, n_groups, q16, q8, scales); break;
+    default: h3::quantize_warp_kernel<4, CODES><<<blocks, 256, 0, s>>>(xb, cols, group, n_groups, q16, q8, scales); break;
+  }
+  return true;
+}
+
 h3dit_status launch_quantize_codes(const void* x, int rows, int cols, int group, void* q, float* scales,
                                    cudaStream_t s) {
   const long long blocks = 1LL * rows * (cols / group);
   if (blocks > 0x7fffffffLL) return fail(H3DIT_E_UNSUPPORTED, "too many groups");
   TimedLaunch tl(kQuant, s);
-  h3::quantize_codes_kernel<<<(unsigned)blocks, h3::kRowThreads, 0, s>>>(static_cast<const bf16*>(x), cols, group,
-                                                                         static_cast<bf16*>(q), scales);
+  if (!launch_quantize_warp<true>(x, rows, cols, group, static_cast<bf16*>(q), nullptr, scales, s))
+    h3::quantize_codes_kernel<<<(unsigned)blocks, h3::kRowThreads, 0, s>>>(static_cast<const bf16*>(x), cols, group,
+                                                                           static_cast<bf16*>(q), scales);
   H3_CUDA(cudaGetLastError());
   return H3DIT_OK;
 }
@@ -927,8 +945,9 @@ h3dit_status h3dit_quantize_act(const void* x_bf16, int rows, int cols, int grou
   const long long blocks = 1LL * rows * (cols / group);
   if (blocks > 0x7fffffffLL) return fail(H3DIT_E_UNSUPPORTED, "too many groups");
   TimedLaunch tl(kQuant, stream);
-  h3::quantize_kernel<<<(unsigned)blocks, h3::kRowThreads, 0, stream>>>(static_cast<const bf16*>(x_bf16), cols, group, q,
-                                                                       scales);
+  if (!launch_quantize_warp<false>(x_bf16, rows, cols, group, nullptr, q, scales, stream))
+    h3::quantize_kernel<<<(unsigned)blocks, h3::kRowThreads, 0, stream>>>(static_cast<const bf16*>(x_bf16), cols, group,
+                                                                         q, scales);
   H3_CUDA(cudaGetLastError());
   return H3DIT_OK;
 }

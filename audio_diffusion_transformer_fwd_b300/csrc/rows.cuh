@@ -36,11 +36,34 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
                     pack_bf16x2(f[6], f[7]));
 }
 
+// A group's quantisation scale s = absmax / 127 and its correctly rounded
+// reciprocal r (0 when s is too small for a normal reciprocal).
+struct QuantScale {
+  float s, r;
+};
+__device__ __forceinline__ QuantScale quant_scale(float s) {
+  QuantScale q;
+  q.s = s;
+  q.r = s >= 0x1p-100f ? __frcp_rn(s) : 0.f;
+  return q;
+}
+
 // int8 code of x at scale s (s = absmax / 127 of x's group): x / s correctly
 // rounded in fp32, rounded half to even, clamped to [-127, 127]; s = 0 gives 0.
-__device__ __forceinline__ int quant_code(float x, float s) {
-  if (s == 0.f) return 0;
-  return max(-127, min(127, __float2int_rn(__fdiv_rn(x, s))));
+// The quotient is formed as t = x * r: |x / s| <= 127.x, so t lies within
+// 128 * 2^-23 (two roundings) of x / s, and the correctly rounded quotient
+// within 2^-24 * 128 of it; both round to the same integer unless t is
+// within 2.3e-5 of a half-integer.  Inside a 1e-4 band around half-integers
+// (rare) the division itself decides.
+__device__ __forceinline__ int quant_code(float x, const QuantScale& q) {
+  if (q.s == 0.f) return 0;
+  float c;
+  const float t = x * q.r;
+  if (q.r != 0.f && fabsf((t - floorf(t)) - 0.5f) > 1e-4f)
+    c = rintf(t);
+  else
+    c = rintf(__fdiv_rn(x, q.s));
+  return max(-127, min(127, static_cast<int>(c)));
 }
 
 // x_out = bf16(x + gate * branch) (if GATE) and h = bf16(LN(x_out)(1+scale)+shift)
@@ -212,8 +235,8 @@ __global__ void __launch_bounds__(kRowThreads, row_min_blocks<GATE, NORM, QUANT,
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
   __syncthreads();
   amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-  const float sq8 = __fdiv_rn(amax, 127.0f);
-  if (threadIdx.x == 0) hs[row] = sq8;
+  const QuantScale sq8 = quant_scale(__fdiv_rn(amax, 127.0f));
+  if (threadIdx.x == 0) hs[row] = sq8.s;
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     const int idx = i * kRowThreads + threadIdx.x;
@@ -254,14 +277,63 @@ __global__ void __launch_bounds__(kRowThreads)
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
   __syncthreads();
   amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-  const float s = __fdiv_rn(amax, 127.0f);
-  if (threadIdx.x == 0) scales[row * groups + g] = s;
+  const QuantScale s = quant_scale(__fdiv_rn(amax, 127.0f));
+  if (threadIdx.x == 0) scales[row * groups + g] = s.s;
   for (int idx = threadIdx.x; idx < nvec; idx += kRowThreads) {
     float f[8];
     unpack8(src[idx], f);
 #pragma unroll
     for (int e = 0; e < 8; ++e) f[e] = static_cast<float>(quant_code(f[e], s));
     dst[idx] = pack8(f);
+  }
+}
+
+// Groups of up to 1024 columns (NV * 256): one warp per group, the group
+// held in registers (NV 16-byte vectors per lane, all loaded before any
+// store, so q may be x), the absmax by warp shuffles.  CODES: the codes as
+// BF16 values into q16, else as int8 into q8.
+template <int NV, bool CODES>
+__global__ void __launch_bounds__(256)
+    quantize_warp_kernel(const __nv_bfloat16* x, int cols, int group, long long n_groups, __nv_bfloat16* q16,
+                         int8_t* q8, float* __restrict__ scales) {
+  const long long gw = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (gw >= n_groups) return;
+  const int lane = threadIdx.x & 31;
+  const int groups = cols / group;
+  const long long row = gw / groups;
+  const int g = static_cast<int>(gw - row * groups);
+  const size_t base = static_cast<size_t>(row) * cols + static_cast<size_t>(g) * group;
+  const uint4* src = reinterpret_cast<const uint4*>(x + base);
+  uint4 u[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) u[i] = src[lane + 32 * i];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    float f[8];
+    unpack8(u[i], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const QuantScale s = quant_scale(__fdiv_rn(amax, 127.0f));
+  if (lane == 0) scales[gw] = s.s;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    float f[8];
+    unpack8(u[i], f);
+    if (CODES) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = static_cast<float>(quant_code(f[e], s));
+      reinterpret_cast<uint4*>(q16 + base)[lane + 32 * i] = pack8(f);
+    } else {
+      uint32_t w[2] = {0u, 0u};
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        w[e >> 2] |= (static_cast<uint32_t>(quant_code(f[e], s)) & 0xFFu) << (8 * (e & 3));
+      reinterpret_cast<uint2*>(q8 + base)[lane + 32 * i] = make_uint2(w[0], w[1]);
+    }
   }
 }
 
@@ -303,8 +375,8 @@ __global__ void __launch_bounds__(kRowThreads)
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
   __syncthreads();
   amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-  const float s = __fdiv_rn(amax, 127.0f);
-  if (threadIdx.x == 0) scales[row * groups + g] = s;
+  const QuantScale s = quant_scale(__fdiv_rn(amax, 127.0f));
+  if (threadIdx.x == 0) scales[row * groups + g] = s.s;
   uint2* dst = reinterpret_cast<uint2*>(q + row * cols + static_cast<size_t>(g) * group);
   for (int idx = threadIdx.x; idx < nvec; idx += kRowThreads) {
     float f[8];

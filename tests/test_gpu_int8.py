@@ -118,7 +118,8 @@ def test_linear_i8_grouped(m, n, k, group):
     assert max_abs(got, ref) <= 2.0 ** -8 * float(np.max(np.abs(ref))) + 1e-6
 
 
-@pytest.mark.parametrize("rows,cols,group", [(64, 1024, 1024), (37, 4096, 1024), (5, 256, 256)])
+@pytest.mark.parametrize("rows,cols,group", [(64, 1024, 1024), (37, 4096, 1024), (5, 256, 256), (9, 5120, 5120),
+                                             (7, 1536, 768)])
 def test_quantize_codes_bit_exact(rows, cols, group):
     x = synth.host_activations(rows, cols, seed=rows) * np.float32(3.0)
     x = synth.to_bf16_values(x)
@@ -136,6 +137,51 @@ def test_quantize_codes_bit_exact(rows, cols, group):
     H.h3dit_check_device_error()
     assert np.array_equal(host(xd).astype(np.int64), qr.astype(np.int64))
     assert np.array_equal(s2.cpu().numpy(), sr)
+
+
+def _quotient_dense_rows(amaxes, cols, seed):
+    """One row per amax: amax and -amax, then BF16 values in
+    (amax * 2^-9, amax] of both signs, so the quotients x / s are dense.  With
+    amax = 127 * 2^e the scale is 2^e and every x = (k + 1/2) * 2^e is an
+    exact tie; other amax values put many quotients next to half-integers."""
+    rng = np.random.default_rng(seed)
+    bits = np.arange(0x0080, 0x7F80, dtype=np.uint32)     # positive normal BF16 values
+    vals = (bits << 16).view(np.float32)
+    half = cols // 2 - 1
+    rows = []
+    for a in amaxes:
+        cand = vals[(vals <= a) & (vals > a * np.float32(2.0 ** -9))]
+        pick = rng.choice(cand, size=half, replace=len(cand) < half)
+        rows.append(rng.permutation(np.concatenate([[a, -a], pick, -pick])))
+    return np.stack(rows).astype(np.float32)
+
+
+@pytest.mark.parametrize("cols,group", [(1024, 1024), (2048, 2048), (1024, 256)])
+def test_quantize_ties_and_near_ties_bit_exact(cols, group):
+    """The quantisers form x / s as x times the reciprocal of s and fall back
+    to the division within 1e-4 of a half-integer; exact ties (round half to
+    even) and near-ties must give the oracle's codes, through the one-warp
+    (group <= 1024) and one-CTA (larger groups) kernels, int8 and BF16 codes,
+    and for a scale too small for a normal reciprocal."""
+    amaxes = [np.float32(v) for v in O.bf16_round(
+        np.array([127.0, 15.875, 127.0 * 2 ** -20, 96.0, 100.0, 1.0, 0.3, 5e-3, 3.3e38, 1e-30]))]
+    x = _quotient_dense_rows(amaxes, cols, seed=cols + group)
+    rows = x.shape[0]
+    qr, sr = O.quantize_rows(x, group)
+    xd = dev_bf16(x)
+    q8 = torch.empty((rows, cols), device="cuda", dtype=torch.int8)
+    s8 = torch.empty((rows, cols // group), device="cuda", dtype=torch.float32)
+    H.h3dit_quantize_act(xd, rows, cols, group, q8, s8)
+    q16 = torch.empty_like(xd)
+    s16 = torch.empty_like(s8)
+    H.h3dit_quantize_codes(xd, rows, cols, group, q16, s16)
+    H.h3dit_check_device_error()
+    assert np.array_equal(q8.cpu().numpy(), qr)
+    assert np.array_equal(host(q16).astype(np.int64), qr.astype(np.int64))
+    assert np.array_equal(s8.cpu().numpy(), sr) and np.array_equal(s16.cpu().numpy(), sr)
+    # the rows with power-of-two scales hold exact ties, so round-half-even decided some codes
+    exact = (x[:3] / sr[:3].repeat(group, axis=1)) % 1.0 == 0.5
+    assert exact.sum() > 100
 
 
 def test_widen_codes_exact():
