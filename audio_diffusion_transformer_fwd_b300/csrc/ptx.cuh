@@ -121,12 +121,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // ----------------------------------------------------------------- clusters
-// This CTA's rank within its thread-block cluster.
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
 // Every thread of every CTA of the cluster; orders shared-memory writes
 // before the barrier with reads (local or distributed) after it.
 __device__ __forceinline__ void cluster_sync_all() {

@@ -50,20 +50,29 @@ __device__ __forceinline__ QuantScale quant_scale(float s) {
 
 // int8 code of x at scale s (s = absmax / 127 of x's group): x / s correctly
 // rounded in fp32, rounded half to even, clamped to [-127, 127]; s = 0 gives 0.
-// The quotient is formed as t = x * r: |x / s| <= 127.x, so t lies within
-// 128 * 2^-23 (two roundings) of x / s, and the correctly rounded quotient
-// within 2^-24 * 128 of it; both round to the same integer unless t is
-// within 2.3e-5 of a half-integer.  Inside a 1e-4 band around half-integers
-// (rare) the division itself decides.
-__device__ __forceinline__ int quant_code(float x, const QuantScale& q) {
-  if (q.s == 0.f) return 0;
-  float c;
+// Returned as a float holding the integer.  The quotient is formed as
+// t = x * r: |x / s| <= 127.x, so t lies within 128 * 2^-23 (two roundings)
+// of x / s, and the correctly rounded quotient within 2^-24 * 128 of it; both
+// round to the same integer unless t is within 2.3e-5 of a half-integer.
+// Where t is within 1e-4 of one (|t - rint(t)| >= 0.4999, rare) the division
+// itself decides.
+__device__ __forceinline__ float quant_code(float x, const QuantScale& q) {
+  if (q.s == 0.f) return 0.f;
   const float t = x * q.r;
-  if (q.r != 0.f && fabsf((t - floorf(t)) - 0.5f) > 1e-4f)
-    c = rintf(t);
-  else
-    c = rintf(__fdiv_rn(x, q.s));
-  return max(-127, min(127, static_cast<int>(c)));
+  float c = rintf(t);
+  if (q.r == 0.f || fabsf(t - c) >= 0.4999f) c = rintf(__fdiv_rn(x, q.s));
+  return fminf(127.f, fmaxf(-127.f, c));
+}
+
+// max |v| over 8 BF16 values, exact (taken on the BF16 pairs).
+__device__ __forceinline__ __nv_bfloat162 absmax8(const uint4 u, __nv_bfloat162 m) {
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m = __hmax2(m, __habs2(b[i]));
+  return m;
+}
+__device__ __forceinline__ float absmax_of(__nv_bfloat162 m) {
+  return fmaxf(__bfloat162float(m.x), __bfloat162float(m.y));
 }
 
 // x_out = bf16(x + gate * branch) (if GATE) and h = bf16(LN(x_out)(1+scale)+shift)
@@ -245,7 +254,7 @@ __global__ void __launch_bounds__(kRowThreads, row_min_blocks<GATE, NORM, QUANT,
       pv.get(i, v);
       float c[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) c[e] = static_cast<float>(quant_code(v[e], sq8));
+      for (int e = 0; e < 8; ++e) c[e] = quant_code(v[e], sq8);
       hr[idx] = pack8(c);   // integers in [-127, 127]: exact in BF16
     }
   }
@@ -265,13 +274,9 @@ __global__ void __launch_bounds__(kRowThreads)
   const uint4* src = reinterpret_cast<const uint4*>(x + base);
   uint4* dst = reinterpret_cast<uint4*>(q + base);
   const int nvec = group >> 3;
-  float amax = 0.f;
-  for (int idx = threadIdx.x; idx < nvec; idx += kRowThreads) {
-    float f[8];
-    unpack8(src[idx], f);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
-  }
+  __nv_bfloat162 m2 = __float2bfloat162_rn(0.f);
+  for (int idx = threadIdx.x; idx < nvec; idx += kRowThreads) m2 = absmax8(src[idx], m2);
+  float amax = absmax_of(m2);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
@@ -283,7 +288,7 @@ __global__ void __launch_bounds__(kRowThreads)
     float f[8];
     unpack8(src[idx], f);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) f[e] = static_cast<float>(quant_code(f[e], s));
+    for (int e = 0; e < 8; ++e) f[e] = quant_code(f[e], s);
     dst[idx] = pack8(f);
   }
 }
@@ -307,14 +312,10 @@ __global__ void __launch_bounds__(256)
   uint4 u[NV];
 #pragma unroll
   for (int i = 0; i < NV; ++i) u[i] = src[lane + 32 * i];
-  float amax = 0.f;
+  __nv_bfloat162 m2 = __float2bfloat162_rn(0.f);
 #pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    float f[8];
-    unpack8(u[i], f);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
-  }
+  for (int i = 0; i < NV; ++i) m2 = absmax8(u[i], m2);
+  float amax = absmax_of(m2);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   const QuantScale s = quant_scale(__fdiv_rn(amax, 127.0f));
@@ -325,13 +326,13 @@ __global__ void __launch_bounds__(256)
     unpack8(u[i], f);
     if (CODES) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) f[e] = static_cast<float>(quant_code(f[e], s));
+      for (int e = 0; e < 8; ++e) f[e] = quant_code(f[e], s);
       reinterpret_cast<uint4*>(q16 + base)[lane + 32 * i] = pack8(f);
     } else {
       uint32_t w[2] = {0u, 0u};
 #pragma unroll
       for (int e = 0; e < 8; ++e)
-        w[e >> 2] |= (static_cast<uint32_t>(quant_code(f[e], s)) & 0xFFu) << (8 * (e & 3));
+        w[e >> 2] |= (static_cast<uint32_t>(static_cast<int>(quant_code(f[e], s))) & 0xFFu) << (8 * (e & 3));
       reinterpret_cast<uint2*>(q8 + base)[lane + 32 * i] = make_uint2(w[0], w[1]);
     }
   }
@@ -363,13 +364,9 @@ __global__ void __launch_bounds__(kRowThreads)
   const int g = blockIdx.x - static_cast<int>(row) * groups;
   const uint4* src = reinterpret_cast<const uint4*>(x + row * cols + static_cast<size_t>(g) * group);
   const int nvec = group >> 3;
-  float amax = 0.f;
-  for (int idx = threadIdx.x; idx < nvec; idx += kRowThreads) {
-    float f[8];
-    unpack8(src[idx], f);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
-  }
+  __nv_bfloat162 m2 = __float2bfloat162_rn(0.f);
+  for (int idx = threadIdx.x; idx < nvec; idx += kRowThreads) m2 = absmax8(src[idx], m2);
+  float amax = absmax_of(m2);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
@@ -384,7 +381,7 @@ __global__ void __launch_bounds__(kRowThreads)
     uint32_t w[2] = {0u, 0u};
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const int c = quant_code(f[e], s);
+      const int c = static_cast<int>(quant_code(f[e], s));
       w[e >> 2] |= (static_cast<uint32_t>(c) & 0xFFu) << (8 * (e & 3));
     }
     dst[idx] = make_uint2(w[0], w[1]);
