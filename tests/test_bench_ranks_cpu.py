@@ -53,3 +53,25 @@ def test_single_process_needs_no_collective():
     r.barrier()
     assert r.max(3.5) == 3.5
     assert r.throughput(10.0, 2.0) == pytest.approx(5000.0)
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` (the fp64 oracle on the host cores, one
+    process, no GPU) prints one JSON line with every key of the bench
+    contract, marked as the reference arm."""
+    import json
+    import subprocess
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                          "--warmup", "0"], cwd=ROOT, capture_output=True, text=True, timeout=600, check=True)
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    j = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in j, key
+    assert j["impl"] == "reference" and j["value"] > 0 and j["higher_is_better"] is True
+    assert j["n_gpus"] == 1 and j["steps"] == 1 and j["warmup"] == 0
+    assert j["cpu_baseline"]["kind"] == "oracle" and j["cpu_baseline"]["cores"] >= 1
+    assert j["e2e"]["h2d_bytes_per_step"] == 0 and j["e2e"]["d2h_bytes_per_step"] == 0
+    assert j["e2e"]["value"] == j["value"] and j["cpu_baseline"]["value"] == j["value"]
+    assert "workload" in j["config"]
