@@ -52,6 +52,20 @@ MUTATIONS = [
     ("block_forward_int8", 'if "qkv" in which:', 'if "o" in which:', [P.test_int8_block_without_int8_projections_is_the_float_block]),
     ("block_forward_int8", 'fc2_int8(uq, us, w["q2"], w["s2"], g2)', 'fc2_int8(uq, us, w["q2"], w["s1"][:w["q2"].shape[0]], g2)',
      [P.test_int8_block_close_to_float_block, P.test_int8_block_without_int8_projections_is_the_float_block]),
+    # int8 quantisation points and granularity
+    ("block_forward_int8", 'oq, os_ = quantize_rows(o)\n        a = R(linear_int8(oq, os_, w["q_o"], w["s_o"]))',
+     'oq, os_ = quantize_rows(o, g2)\n        a = R(fc2_int8(oq, os_, w["q_o"], w["s_o"], g2))',
+     [P.test_int8_block_scalar_loops]),
+    ("block_forward_int8", "oq, os_ = quantize_rows(o)", "oq, os_ = quantize_rows(_merge_heads(attention(q, k, v, rows=rows)))",
+     [P.test_int8_block_scalar_loops]),
+    ("block_forward_int8", "h2q, h2s = quantize_rows(h2)", "h2q, h2s = quantize_rows(adaln(x1, shift2, scale2, cfg.eps))",
+     [P.test_int8_block_scalar_loops]),
+    ("block_forward_int8", "hq, hs = quantize_rows(h)", "hq, hs = quantize_rows(adaln(x, shift1, scale1, cfg.eps))",
+     [P.test_int8_block_scalar_loops]),
+    ("block_forward_int8", "uq, us = quantize_rows(u, g2)",
+     'uq, us = quantize_rows(linear_int8(h2q, h2s, w["q1"], w["s1"]), g2)', [P.test_int8_block_scalar_loops]),
+    ("fc2_int8", "out += us[:, g:g + 1] * acc", "out += us.max(axis=1, keepdims=True) * acc",
+     [P.test_int8_block_scalar_loops]),
     # per-segment modulation
     ("segment_mod", "seg[starts[s_]:starts[s_ + 1]] = s_", "seg[starts[s_]:starts[s_ + 1]] = min(s_, 1)",
      [P.test_segment_mod_equals_per_segment_blocks]),

@@ -504,6 +504,149 @@ def test_int8_block_without_int8_projections_is_the_float_block():
     assert errs[O.INT8_ALL] > max(errs[O.INT8_QKV], errs[O.INT8_MLP])
 
 
+# A block small enough for scalar loops whose widths span several FC2 groups:
+# with d = 16, F = 32 and a group of 8, a per-token scale (one per row of 16
+# or 32) and a per-group scale (one per 8 channels) are different things, so
+# quantising a tensor at the wrong granularity changes its codes.
+TINY8 = O.BlockConfig(d=16, heads=2, head_dim=8, ffn=32, eps=1e-6, rope_sections=(2, 2, 4))
+TINY8_GROUP = 8
+
+
+def _bf16_list(vals):
+    """BF16 storage of fp64 values through torch's casts (binary64 -> binary32
+    -> bfloat16, each rounding to nearest even), back as Python floats."""
+    t = torch.tensor(list(vals), dtype=torch.float64).to(torch.float32).to(torch.bfloat16)
+    return t.double().tolist()
+
+
+def _quant_loops(vals):
+    """The int8 rule written out for one group of values: s = absmax / 127
+    divided in binary32, code = the binary32 quotient x / s rounded half to
+    even (Python's round) and clamped to +-127; an all-zero group has s = 0
+    and codes 0.  Returns (codes as Python ints, s as a Python float)."""
+    amax = np.float32(max(abs(v) for v in vals))
+    s = np.float32(amax / np.float32(127.0))
+    if s == 0:
+        return [0] * len(vals), 0.0
+    codes = [max(-127, min(127, round(float(np.float32(np.float32(v) / s))))) for v in vals]
+    return codes, float(s)
+
+
+def _block_int8_loops(x, w, mod, pos, cfg, group):
+    """The dynamic-int8 block ([linlog] "int8 量化：从 36 秒到 19 秒") written
+    out element by element with every quantisation point spelled out: h, o
+    and h2 are stored as BF16 and then quantised per token; FC1's GELU output
+    u is stored as BF16 and quantised per token and per ``group`` channels;
+    each projection is an exact integer sum (Python ints) dequantised as
+    acc * s_act * s_w, FC2 as s_w * sum over groups (ascending) of
+    s_u[group] * acc_group; every stored tensor is BF16.  Returns the output
+    and the codes and scales of the four quantised tensors."""
+    n, d = x.shape
+    H, Dh, F = cfg.heads, cfg.head_dim, cfg.ffn
+    sh1, sc1, g1, sh2, sc2, g2 = mod
+
+    def ln_row(row, shift, scale):
+        mu = sum(row) / d
+        var = sum((a - mu) ** 2 for a in row) / d
+        return [(row[c] - mu) / math.sqrt(var + cfg.eps) * (1 + scale[c]) + shift[c] for c in range(d)]
+
+    def rot(vec, p):
+        out = list(vec)
+        start = 0
+        for axis, sec in enumerate(cfg.rope_sections):
+            for i in range(sec // 2):
+                ang = p[axis] * cfg.rope_theta ** (-2.0 * i / sec)
+                a, b = vec[start + 2 * i], vec[start + 2 * i + 1]
+                out[start + 2 * i] = a * math.cos(ang) - b * math.sin(ang)
+                out[start + 2 * i + 1] = a * math.sin(ang) + b * math.cos(ang)
+            start += sec
+        return out
+
+    def qlinear(codes, s_act, wq, ws):
+        acc = [sum(codes[c] * int(wq[o][c]) for c in range(len(codes))) for o in range(len(wq))]
+        return [acc[o] * s_act * float(ws[o]) for o in range(len(wq))]
+
+    h = [_bf16_list(ln_row(x[t], sh1, sc1)) for t in range(n)]
+    hq = [_quant_loops(h[t]) for t in range(n)]
+    qkv = [qlinear(hq[t][0], hq[t][1], w["q_qkv"], w["s_qkv"]) for t in range(n)]
+    Q = [[_bf16_list(rot(qkv[t][hd * Dh:(hd + 1) * Dh], pos[t])) for t in range(n)] for hd in range(H)]
+    K = [[_bf16_list(rot(qkv[t][d + hd * Dh:d + (hd + 1) * Dh], pos[t])) for t in range(n)] for hd in range(H)]
+    V = [[_bf16_list(qkv[t][2 * d + hd * Dh:2 * d + (hd + 1) * Dh]) for t in range(n)] for hd in range(H)]
+    o = [[0.0] * d for _ in range(n)]
+    for hd in range(H):
+        for i in range(n):
+            s = [sum(Q[hd][i][c] * K[hd][j][c] for c in range(Dh)) / math.sqrt(Dh) for j in range(n)]
+            mx = max(s)
+            e = [math.exp(z - mx) for z in s]
+            tot = sum(e)
+            for c in range(Dh):
+                o[i][hd * Dh + c] = sum(e[j] / tot * V[hd][j][c] for j in range(n))
+    o = [_bf16_list(row) for row in o]
+    oq, h2q, uq, out = [], [], [], []
+    for t in range(n):
+        oq.append(_quant_loops(o[t]))
+        a = _bf16_list(qlinear(oq[t][0], oq[t][1], w["q_o"], w["s_o"]))
+        x1 = _bf16_list([x[t][c] + g1[c] * a[c] for c in range(d)])
+        h2 = _bf16_list(ln_row(x1, sh2, sc2))
+        h2q.append(_quant_loops(h2))
+        pre = qlinear(h2q[t][0], h2q[t][1], w["q1"], w["s1"])
+        u = _bf16_list([0.5 * z * (1 + math.tanh(math.sqrt(2 / math.pi) * (z + 0.044715 * z ** 3))) for z in pre])
+        groups = [_quant_loops(u[g0:g0 + group]) for g0 in range(0, F, group)]
+        uq.append(groups)
+        m = []
+        for c in range(d):
+            tot = 0.0
+            for gi, (codes, su) in enumerate(groups):
+                acc = sum(codes[j] * int(w["q2"][c][gi * group + j]) for j in range(group))
+                tot += su * acc
+            m.append(float(w["s2"][c]) * tot)
+        m = _bf16_list(m)
+        out.append(_bf16_list([x1[c] + g2[c] * m[c] for c in range(d)]))
+    return np.array(out), dict(hq=hq, oq=oq, h2q=h2q, uq=uq)
+
+
+def _tiny8_inputs(seed, n=5):
+    r = np.random.default_rng(seed)
+    d, f = TINY8.d, TINY8.ffn
+    w = {}
+    for name, qn, sn, shp in (("w_qkv", "q_qkv", "s_qkv", (3 * d, d)), ("w_o", "q_o", "s_o", (d, d)),
+                              ("w1", "q1", "s1", (f, d)), ("w2", "q2", "s2", (d, f))):
+        # per-channel magnitudes that differ across each row, so group and
+        # token absmax differ
+        wt = r.standard_normal(shp) * 0.3 * r.uniform(0.2, 3.0, (1, shp[1]))
+        w[qn], s = O.quantize_weight(wt)
+        w[sn] = s[:, 0]
+    mod = r.standard_normal((6, d)) * 0.5
+    x = O.bf16_round(r.standard_normal((n, d)) * r.uniform(0.2, 3.0, (1, d)))
+    pos = r.uniform(0, 9, (n, 3))
+    return x, w, mod, pos
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_int8_block_scalar_loops(seed):
+    """The oracle's int8 block against the element-by-element restatement on
+    a block whose widths span several FC2 groups: every code and scale of h,
+    o, h2 (per token) and u (per token and group) equal, and the outputs
+    equal to rounding."""
+    x, w, mod, pos = _tiny8_inputs(seed)
+    got, parts = O.block_forward_int8(x, w, mod, pos, TINY8, bf16_storage=True, fc2_group=TINY8_GROUP,
+                                      return_parts=True)
+    want, lp = _block_int8_loops(x, w, mod, pos, TINY8, TINY8_GROUP)
+    for name, qn, sn in (("h", "hq", "hs"), ("o", "oq", "os"), ("h2", "h2q", "h2s")):
+        codes = np.array([c for c, _ in lp[qn]])
+        scales = np.array([s for _, s in lp[qn]])
+        assert np.array_equal(parts[qn].astype(np.int64), codes), f"{name} codes"
+        assert np.array_equal(parts[sn][:, 0].astype(np.float64), scales), f"{name} scales"
+    ucodes = np.array([[c for codes, _ in row for c in codes] for row in lp["uq"]])
+    uscales = np.array([[s for _, s in row] for row in lp["uq"]])
+    assert parts["us"].shape == (x.shape[0], TINY8.ffn // TINY8_GROUP)
+    assert np.array_equal(parts["uq"].astype(np.int64), ucodes), "u codes"
+    assert np.array_equal(parts["us"].astype(np.float64), uscales), "u scales"
+    assert np.allclose(got, want, rtol=0, atol=1e-12)
+    # the group and per-token scales really differ on this block
+    assert not np.allclose(uscales, uscales.max(axis=1, keepdims=True))
+
+
 # ------------------------------------------------------------------ per-segment modulation
 
 
