@@ -48,6 +48,10 @@ struct GemmArgs {
   int d;
   int head_dim;
   const float2* rope;  // [M][head_dim/2] (cos, sin)
+  // Test hook, -1 in every normal launch: the producer of CTA 0 stops before
+  // k-block `stall_kb` of its first tile and issues nothing more, so the MMA
+  // thread's wait on that stage runs out (see h3dit_test_stall_next_gemm).
+  int stall_kb;
 };
 
 __device__ __forceinline__ float gelu_tanh_f(float x) {
@@ -167,10 +171,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      const int stall_kb = blockIdx.x == 0 ? args.stall_kb : -1;
       for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
         int mb, nb;
         gemm_tile_coords(t, args, mb, nb);
         for (int kb = 0; kb < kblocks; ++kb) {
+          if (t == blockIdx.x && kb == stall_kb) { ok = false; break; }
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
           const uint32_t fb = full0 + 8 * stage;
           mbar_arrive_expect_tx(fb, kGemmStageBytes);

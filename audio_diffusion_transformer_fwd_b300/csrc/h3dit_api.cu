@@ -3,8 +3,10 @@
 // this one translation unit (the kernel files are included below).
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -50,6 +52,43 @@ h3dit_status fail(h3dit_status st, const char* fmt, ...) {
     h3dit_status s_ = (expr);              \
     if (s_ != H3DIT_OK) return s_;         \
   } while (0)
+
+// ------------------------------------------------------------------ fault injection
+// H3DIT_FAULT=alloc|launch|arg|shape makes the block and step entry points
+// fail on purpose, on the host, at the point where that failure would
+// arise: alloc = the workspace is too small (E_NOMEM), arg = an argument is
+// invalid (E_INVAL), shape = the shape is unsupported (E_UNSUPPORTED),
+// launch = the first kernel launch fails (E_CUDA, nothing enqueued).  It
+// exists to test how callers see errors; no GPU is made to fault.
+enum FaultKind { kFaultNone = 0, kFaultAlloc, kFaultLaunch, kFaultArg, kFaultShape };
+
+FaultKind injected_fault() {
+  const char* e = getenv("H3DIT_FAULT");
+  if (!e || !e[0]) return kFaultNone;
+  if (!strcmp(e, "alloc")) return kFaultAlloc;
+  if (!strcmp(e, "launch")) return kFaultLaunch;
+  if (!strcmp(e, "arg")) return kFaultArg;
+  if (!strcmp(e, "shape")) return kFaultShape;
+  return kFaultNone;
+}
+
+// The next BF16 GEMM launch (any thread) gets this k-block as its stall
+// point (h3dit_test_stall_next_gemm); -1 = none.
+std::atomic<int> g_stall_request{-1};
+int take_stall_request() { return g_stall_request.exchange(-1); }
+
+// ------------------------------------------------------------------ tracing
+// NVTX ranges around every block and step (free unless a profiler that
+// records NVTX is attached): "h3dit block b" nests inside "h3dit step".
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  NvtxRange(const char* prefix, int index) {
+    char buf[48];
+    snprintf(buf, sizeof(buf), "%s %d", prefix, index);
+    nvtxRangePushA(buf);
+  }
+  ~NvtxRange() { nvtxRangePop(); }
+};
 
 // ------------------------------------------------------------------ timing
 enum KernelClass { kRows = 0, kQKV = 1, kAttn = 2, kOProj = 3, kFC1 = 4, kFC2 = 5, kReduce = 6, kQuant = 7, kNumClasses = 8 };
@@ -255,6 +294,7 @@ h3dit_status gemm_setup(const void* A, const void* B, int M, int N, int K, CUten
   args.M = M;
   args.N = N;
   args.K = K;
+  args.stall_kb = -1;
   args.tiles_m = (M + h3::kGemmBM - 1) / h3::kGemmBM;
   args.tiles_n = N / h3::kGemmBN;
   args.num_tiles = args.tiles_m * args.tiles_n;
@@ -265,6 +305,8 @@ h3dit_status launch_gemm(int epi, const void* A, const void* B, int M, int N, in
                          int cls, cudaStream_t s) {
   CUtensorMap ta, tb;
   H3_TRY(gemm_setup(A, B, M, N, K, ta, tb, args));
+  args.stall_kb = take_stall_request();
+  if (args.stall_kb >= args.K / h3::kGemmBK) args.stall_kb = -1;
   const int grid = std::min(args.num_tiles, sm_count());
   TimedLaunch tl(cls, s);
   switch (epi) {
@@ -478,6 +520,7 @@ h3dit_status launch_quantize_codes(const void* x, int rows, int cols, int group,
 }
 
 h3dit_status launch_rope_table(const h3dit_config* c, const float* pos, int n, float* table, cudaStream_t s) {
+  if (injected_fault() == kFaultLaunch) return fail(H3DIT_E_CUDA, "injected launch failure (H3DIT_FAULT=launch)");
   TimedLaunch tl(kRows, s);
   h3::RopeSpec rs;
   rs.head_dim = c->head_dim;
@@ -673,6 +716,18 @@ h3dit_status h3dit_check_device_error(cudaStream_t stream) {
   return H3DIT_OK;
 }
 
+h3dit_status h3dit_test_set_wait_limit(unsigned long long ns) {
+  const unsigned long long v = ns ? ns : h3::kWaitLimitNs;
+  H3_CUDA(cudaMemcpyToSymbol(h3::g_wait_limit_ns, &v, sizeof(v)));
+  return H3DIT_OK;
+}
+
+h3dit_status h3dit_test_stall_next_gemm(int kblock) {
+  if (kblock < -1) return fail(H3DIT_E_INVAL, "kblock %d", kblock);
+  g_stall_request.store(kblock);
+  return H3DIT_OK;
+}
+
 h3dit_status h3dit_timing_enable(int on) {
   std::lock_guard<std::mutex> lk(g_timing.mu);
   g_timing.enabled = on != 0;
@@ -790,18 +845,24 @@ static h3dit_status block_forward_impl(const h3dit_config* cfg, const h3dit_bloc
                                 const h3dit_segments* seg, void* x, const float* pos, int n_tokens, void* ws,
                                 size_t ws_bytes, cudaStream_t stream) {
   H3_TRY(check_cfg(cfg));
+  const FaultKind fk = injected_fault();
+  if (fk == kFaultShape) return fail(H3DIT_E_UNSUPPORTED, "injected unsupported shape (H3DIT_FAULT=shape)");
   H3_TRY(check_weights(cfg, w));
   if (!mod || !x || !pos || !ws) return fail(H3DIT_E_INVAL, "NULL pointer");
+  if (fk == kFaultArg) return fail(H3DIT_E_INVAL, "injected invalid argument (H3DIT_FAULT=arg)");
   if (n_tokens < 1) return fail(H3DIT_E_INVAL, "n_tokens %d", n_tokens);
   if (!aligned(ws, 256) || !aligned(x, 16)) return fail(H3DIT_E_INVAL, "ws must be 256-byte and x 16-byte aligned");
   h3::SegMap sm;
   H3_TRY(make_segmap(seg, n_tokens, cfg->d, &sm));
   const Arena ar = plan_arena(cfg, n_tokens, nullptr);
-  if (ws_bytes < ar.total) return fail(H3DIT_E_NOMEM, "workspace %zu < %zu bytes", ws_bytes, ar.total);
+  if (ws_bytes < ar.total || fk == kFaultAlloc)
+    return fail(H3DIT_E_NOMEM, "workspace %zu < %zu bytes%s", ws_bytes, ar.total,
+                fk == kFaultAlloc ? " (injected: H3DIT_FAULT=alloc)" : "");
   BlockBufs B{static_cast<uint8_t*>(ws), ar};
   float* rope = reinterpret_cast<float*>(B.base + ar.rope);
   bf16* xb = static_cast<bf16*>(x);
   const int d = cfg->d;
+  NvtxRange trace("h3dit block");
   H3_TRY(launch_rope_table(cfg, pos, n_tokens, rope, stream));
   float* hs = int8_set(cfg->precision).qkv ? reinterpret_cast<float*>(B.base + ar.sc_row) : nullptr;
   H3_TRY(launch_rows(xb, nullptr, nullptr, mod + 0 * d, mod + 1 * d, B.base + ar.a2, hs, n_tokens, d, cfg->eps,
@@ -813,10 +874,13 @@ static h3dit_status step_forward_impl(const h3dit_config* cfg, const h3dit_block
                                const float* mods, const h3dit_segments* seg, void* x, const float* pos, int n_tokens,
                                const h3dit_reduction* tr, void* ws, size_t ws_bytes, cudaStream_t stream) {
   H3_TRY(check_cfg(cfg));
+  const FaultKind fk = injected_fault();
+  if (fk == kFaultShape) return fail(H3DIT_E_UNSUPPORTED, "injected unsupported shape (H3DIT_FAULT=shape)");
   if (!w || n_blocks < 0) return fail(H3DIT_E_INVAL, "weights NULL or n_blocks < 0");
   if (n_blocks == 0) return H3DIT_OK;
   for (int b = 0; b < n_blocks; ++b) H3_TRY(check_weights(cfg, &w[b]));
   if (!mods || !x || !pos || !ws) return fail(H3DIT_E_INVAL, "NULL pointer");
+  if (fk == kFaultArg) return fail(H3DIT_E_INVAL, "injected invalid argument (H3DIT_FAULT=arg)");
   if (n_tokens < 1) return fail(H3DIT_E_INVAL, "n_tokens %d", n_tokens);
   if (!aligned(ws, 256) || !aligned(x, 16)) return fail(H3DIT_E_INVAL, "ws must be 256-byte and x 16-byte aligned");
   if (tr) {
@@ -830,11 +894,14 @@ static h3dit_status step_forward_impl(const h3dit_config* cfg, const h3dit_block
   if (tr) H3_TRY(reduce_segmap(sm_full, pair_grid(&tr->grid, n_tokens), &sm_red));
   const size_t per_block = (size_t)sm_full.count * 6 * cfg->d;   // modulation floats per block
   const Arena ar = plan_arena(cfg, n_tokens, tr);
-  if (ws_bytes < ar.total) return fail(H3DIT_E_NOMEM, "workspace %zu < %zu bytes", ws_bytes, ar.total);
+  if (ws_bytes < ar.total || fk == kFaultAlloc)
+    return fail(H3DIT_E_NOMEM, "workspace %zu < %zu bytes%s", ws_bytes, ar.total,
+                fk == kFaultAlloc ? " (injected: H3DIT_FAULT=alloc)" : "");
   BlockBufs B{static_cast<uint8_t*>(ws), ar};
   const int d = cfg->d;
   bf16* xfull = static_cast<bf16*>(x);
   float* rope_full = reinterpret_cast<float*>(B.base + ar.rope);
+  NvtxRange trace("h3dit step");
   H3_TRY(launch_rope_table(cfg, pos, n_tokens, rope_full, stream));
 
   h3::PairGrid pg{};
@@ -870,6 +937,7 @@ static h3dit_status step_forward_impl(const h3dit_config* cfg, const h3dit_block
     const float* nmod = last ? nullptr : mods + per_block * (b + 1);
     const bool emit_next = !last && !reduce_now && !restore_now;
     const int vt_ld = (int)round_up((size_t)cur_n, 64);
+    NvtxRange block_trace("h3dit block", b);
     H3_TRY(run_block_body(cfg, &w[b], mod, cur, cur_n, cur_rope, B, vt_ld,
                           emit_next ? nmod : nullptr, emit_next ? nmod + d : nullptr, stream, *cur_sm));
     if (reduce_now) {
@@ -1223,9 +1291,11 @@ std::mutex g_static_mu;
 void* g_static_addr[64] = {nullptr};
 
 // Device address of g_static_scratch on the current device, looked up once
-// per device.  On the host the array's name only stands in for the symbol;
+// per device (the first call on that device) and kept for the life of the
+// process.  On the host the array's name only stands in for the symbol;
 // passing it to a kernel would be wrong, so the real address comes from the
-// runtime.
+// runtime.  cudaDeviceReset unloads the module, so the kept address is not
+// valid after one: the header says a reset ends the use of this entry point.
 h3dit_status static_scratch_address(void** out) {
   int dev = -1;
   H3_CUDA(cudaGetDevice(&dev));
@@ -1246,8 +1316,13 @@ h3dit_status static_scratch_address(void** out) {
 extern "C" h3dit_status h3dit_block_forward_noalloc(const h3dit_config* cfg, const h3dit_block_weights* w,
                                                     const float* mod, void* x, const float* pos, int n_tokens,
                                                     cudaStream_t stream) {
+  // the same argument checks as h3dit_block_forward, in the same order,
+  // before the size of the built-in scratch is considered
   H3_TRY(check_cfg(cfg));
+  H3_TRY(check_weights(cfg, w));
+  if (!mod || !x || !pos) return fail(H3DIT_E_INVAL, "NULL pointer");
   if (n_tokens < 1) return fail(H3DIT_E_INVAL, "n_tokens %d", n_tokens);
+  if (!aligned(x, 16)) return fail(H3DIT_E_INVAL, "x must be 16-byte aligned");
   const size_t need = plan_arena(cfg, n_tokens, nullptr).total;
   if (need > kStaticScratchBytes)
     return fail(H3DIT_E_NOMEM,

@@ -15,8 +15,11 @@ __device__ unsigned int g_device_error = 0;
 
 constexpr unsigned int kErrTimeout = 1u;
 // A legitimate wait in these kernels lasts microseconds; 2 s means the
-// pipeline is stuck.
+// pipeline is stuck.  The limit lives in device memory so that a test can
+// shorten it (h3dit_test_set_wait_limit) and watch a stalled pipeline give
+// up within milliseconds.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+__device__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -57,7 +60,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase of parity `parity` has completed.  Bounded: after
-// kWaitLimitNs (or once another role of the CTA gave up and raised *abort)
+// g_wait_limit_ns (or once another role of the CTA gave up and raised *abort)
 // it records the timeout and returns false so the caller can unwind.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -67,7 +70,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     for (int i = 0; i < 256; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > g_wait_limit_ns) {
       *abort = 1;
       atomicOr(&g_device_error, kErrTimeout);
       return false;

@@ -35,6 +35,7 @@ _EXPORTS = [
     "h3dit_attention", "h3dit_linear",
     "h3dit_quantize_codes", "h3dit_widen_codes", "h3dit_linear_i8", "h3dit_linear_i8_acc",
     "h3dit_adaln_quant", "h3dit_gate_residual_adaln_quant", "h3dit_qkv_project_i8",
+    "h3dit_test_set_wait_limit", "h3dit_test_stall_next_gemm",
 ]
 
 
@@ -91,6 +92,8 @@ def lib():
             "h3dit_last_error": (ctypes.c_char_p, []),
             "h3dit_version": (i, []),
             "h3dit_check_device_error": (i, [vp]),
+            "h3dit_test_set_wait_limit": (i, [ctypes.c_ulonglong]),
+            "h3dit_test_stall_next_gemm": (i, [i]),
             "h3dit_timing_enable": (i, [i]),
             "h3dit_timing_reset": (i, []),
             "h3dit_timing_read": (i, [i, P(ctypes.c_double), P(ctypes.c_longlong)]),
@@ -206,6 +209,17 @@ def h3dit_version() -> int:
 
 def h3dit_check_device_error(stream=None):
     _check(lib().h3dit_check_device_error(_stream(stream)))
+
+
+def h3dit_test_set_wait_limit(ns: int):
+    """Device-side limit of every pipeline wait, in ns (0 = the default 2 s)."""
+    _check(lib().h3dit_test_set_wait_limit(ns))
+
+
+def h3dit_test_stall_next_gemm(kblock: int):
+    """Make the next BF16 projection's first CTA stop loading at ``kblock``
+    (its wait then runs out; -1 cancels)."""
+    _check(lib().h3dit_test_stall_next_gemm(kblock))
 
 
 def h3dit_timing_enable(on: bool):

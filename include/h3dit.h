@@ -157,6 +157,34 @@ int h3dit_version(void);
  * if set, H3DIT_E_CUDA if the synchronisation itself failed. */
 h3dit_status h3dit_check_device_error(cudaStream_t stream);
 
+/* ---------------------------------------------------------------- failure testing
+ * Not part of the method (the pages have no counterpart); these let a test
+ * drive the failure paths without faulting or hanging a GPU.
+ *
+ * Host-side injection: with the environment variable H3DIT_FAULT set to
+ * alloc, arg, shape or launch, h3dit_block_forward(_seg) and
+ * h3dit_step_forward(_seg) fail on purpose where that failure would arise
+ * and report E_NOMEM (workspace too small), E_INVAL (invalid argument),
+ * E_UNSUPPORTED (unsupported shape) or E_CUDA (the first launch failed);
+ * nothing is enqueued.  The variable is read at every call.
+ *
+ * h3dit_test_set_wait_limit: the device-side limit of every pipeline wait
+ * on the current device, in nanoseconds (0 restores the default, 2 s).  A
+ * kernel whose wait runs out raises the device error word, lets its own
+ * copies and tensor-core work in flight finish, frees its tensor memory and
+ * returns.  Synchronous (a copy to a device variable).
+ *
+ * h3dit_test_stall_next_gemm: the next BF16 projection launched by the
+ * library (any entry point, any thread) runs with the TMA producer of its
+ * first CTA stopping before k-block `kblock` of its first tile; nothing is
+ * loaded for that stage, so the tensor-core thread's wait on it runs out
+ * after the wait limit and the launch ends with the device error word set
+ * (h3dit_check_device_error then reports E_TIMEOUT, and that launch's
+ * output is invalid).  -1 cancels a pending request; a kblock past the
+ * launch's last k-block is ignored.  E_INVAL for kblock < -1. */
+h3dit_status h3dit_test_set_wait_limit(unsigned long long ns);
+h3dit_status h3dit_test_stall_next_gemm(int kblock);
+
 /* Per-kernel-class timing with CUDA events recorded on the launch stream
  * around every launch while enabled (off by default).  Classes:
  * 0 row kernels, 1 QKV GEMM, 2 attention, 3 out-projection GEMM, 4 FC1 GEMM,
@@ -241,13 +269,17 @@ h3dit_status h3dit_step_forward_seg(const h3dit_config* cfg, const h3dit_block_w
  * the caller still passes x (in/out), weights, mod and pos as above.
  *  - The first call on each device looks up that array's device address
  *    (and so loads the library's device code there); make that first call
- *    before any stream capture.
+ *    before any stream capture.  The address is kept for the life of the
+ *    process: after cudaDeviceReset on a device, do not call this entry
+ *    point on that device again.
  *  - Every call on a device uses the same array, which keeps whatever the
  *    last call left in it (nothing has to start at zero).  Calls that can
  *    overlap on the GPU (other streams, other host threads) race on it:
  *    serialise them.
- *  - Shapes whose workspace (h3dit_workspace_size) exceeds 64 MiB are
- *    refused with H3DIT_E_NOMEM before anything is enqueued.
+ *  - Arguments are checked as h3dit_block_forward checks them (E_INVAL,
+ *    E_UNSUPPORTED) first; then shapes whose workspace
+ *    (h3dit_workspace_size) exceeds 64 MiB are refused with H3DIT_E_NOMEM,
+ *    before anything is enqueued.
  * Other errors as h3dit_block_forward. */
 h3dit_status h3dit_block_forward_noalloc(const h3dit_config* cfg, const h3dit_block_weights* w,
                                          const float* mod, void* x, const float* pos, int n_tokens,

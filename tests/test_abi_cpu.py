@@ -78,3 +78,43 @@ def test_workspace_aliasing_saves_memory():
     got = H.h3dit_workspace_size(shape, n)
     unaliased = 2 * n * (5120 * (1 + 3 + 1 + 1 + 1 + 1) + 20480)   # h, qkv, o, a, h2, m, u
     assert got < 0.8 * unaliased
+
+
+@pytest.mark.parametrize("fault,status,word", [("alloc", H.E_NOMEM, "workspace"), ("arg", H.E_INVAL, "argument"),
+                                               ("shape", H.E_UNSUPPORTED, "shape"), ("launch", H.E_CUDA, "launch")])
+def test_injected_faults_reach_the_caller(lib, monkeypatch, fault, status, word):
+    """H3DIT_FAULT makes the block and step entry points fail where that
+    failure would arise, before anything is enqueued (no GPU is needed: the
+    pointers below are never dereferenced)."""
+    shape = H.BlockShape(256, 4, 64, 1024, 1e-6, (16, 24, 24))
+    fake = 1 << 20                                   # aligned, never dereferenced
+    bw = H.block_weights(fake, fake, fake, fake)
+    n = 256
+    need = H.h3dit_workspace_size(shape, n)
+    g = H.video_grid(0, 2, 8, 12)
+    tr = H.reduction(g, 0, 1)
+    need_tr = H.h3dit_workspace_size(shape, n, tr)
+    monkeypatch.setenv("H3DIT_FAULT", fault)
+    with pytest.raises(H.H3DitError) as e:
+        H.h3dit_block_forward(shape, bw, fake, fake, fake, n, fake, need, stream=0)
+    assert e.value.status == status and word in str(e.value) and "H3DIT_FAULT" in str(e.value)
+    with pytest.raises(H.H3DitError) as e:
+        H.h3dit_step_forward(shape, [bw, bw], fake, fake, fake, n, tr, fake, need_tr, stream=0)
+    assert e.value.status == status and "H3DIT_FAULT" in str(e.value)
+    # genuine argument errors still win over an injected allocation failure
+    if fault == "alloc":
+        with pytest.raises(H.H3DitError) as e:
+            H.h3dit_block_forward(shape, bw, fake, None, fake, n, fake, need, stream=0)
+        assert e.value.status == H.E_INVAL
+    monkeypatch.delenv("H3DIT_FAULT")
+    # a short workspace is refused without any injection
+    with pytest.raises(H.H3DitError) as e:
+        H.h3dit_block_forward(shape, bw, fake, fake, fake, n, fake, need - 256, stream=0)
+    assert e.value.status == H.E_NOMEM
+
+
+def test_stall_request_arguments(lib):
+    with pytest.raises(H.H3DitError) as e:
+        H.h3dit_test_stall_next_gemm(-2)
+    assert e.value.status == H.E_INVAL
+    H.h3dit_test_stall_next_gemm(-1)
