@@ -1,8 +1,12 @@
-// Persistent tcgen05 GEMM for the block's four projections:
+// Persistent tcgen05 GEMMs for the block's four projections:
 //   C[m][n] = epilogue( sum_k A[m][k] * B[n][k] )     A, B BF16, K-major
 // A = activations [M tokens][K], B = a Linear weight [N out][K in].
+// Two kernels compute the same sums in the same order: the CTA-pair kernel
+// at the end of this file (the one the library launches) and the
+// single-CTA kernel below (kept as its A/B reference and for the int8-code
+// variant in gemm_i8.cuh).
 //
-// One CTA per SM walks output tiles of 128 x 256.  Warp 0 streams A/B
+// Single-CTA kernel: one CTA per SM walks output tiles of 128 x 256.  Warp 0 streams A/B
 // k-blocks (64 wide) into a 4-deep shared-memory ring with TMA (128-byte
 // swizzle); one thread of warp 1 issues tcgen05.mma (M=128, N=256, K=16)
 // into one of two fp32 TMEM accumulators; warps 2-5 drain the other
@@ -251,6 +255,178 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, kGemmTmemCols);
+}
+
+}  // namespace h3
+
+namespace h3 {
+
+// ---------------------------------------------------------------------------
+// The same GEMM on CTA pairs (tcgen05 cta_group::2).  A cluster of two CTAs
+// on two SMs computes 256 x 256 output tiles: each CTA streams its own 128 A
+// rows and half (128 rows) of the 256 weight rows of a k-block, and rank 0
+// issues one M = 256, N = 256 MMA per 16 channels that reads both CTAs'
+// shared memory; each CTA's tensor memory receives its own 128 rows.  Per SM
+// a k-block is 32 KB of operands instead of 48 KB, so the same shared memory
+// holds a 6-deep ring (3072 cycles of MMA work in flight instead of 2048)
+// and a third less data crosses L2.  Roles per CTA as in the single-CTA
+// kernel: warp 0 TMA, warp 1 MMA (rank 0 only; both allocate), warps 2-5
+// epilogue.  Stage completion: rank 0 expects both CTAs' bytes on its own
+// full barrier, which both CTAs' copies complete; the MMA commit arrives on
+// the empty (and accumulator-full) barriers of both CTAs; the epilogue
+// threads of both CTAs arrive on rank 0's accumulator-empty barrier.
+constexpr int kPairStages = 6;
+constexpr int kPairRows = 128;                       // A rows and B rows per CTA per tile
+constexpr int kPairABytes = kPairRows * kGemmBK * 2;  // 16 KB
+constexpr int kPairBBytes = kPairRows * kGemmBK * 2;  // 16 KB
+constexpr int kPairStageBytes = kPairABytes + kPairBBytes;
+constexpr size_t kPairSmemBytes = 1024 + kPairStages * kPairStageBytes + 256;
+
+template <int EPI>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                          const GemmArgs args) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kPairStages * kPairABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPairStages * kPairStageBytes);
+  // bars: full[S], empty[S], tfull[2], tempty[2], drain
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kPairStages + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int cluster = blockIdx.x >> 1;
+  const int clusters = gridDim.x >> 1;
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = smem_u32(bars + kPairStages);
+  const uint32_t tfull0 = smem_u32(bars + 2 * kPairStages);
+  const uint32_t tempty0 = smem_u32(bars + 2 * kPairStages + 2);
+  const uint32_t drain = smem_u32(bars + 2 * kPairStages + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(tfull0 + 8 * i, 1);
+      mbar_init(tempty0 + 8 * i, 2 * 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_holder), kGemmTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  // both CTAs' barriers are initialised before either CTA signals the other
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int kblocks = args.K / kGemmBK;
+  const uint32_t full0_lead = mapa_shared(full0, 0);
+  const uint32_t tempty0_lead = mapa_shared(tempty0, 0);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (both CTAs)
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      const int stall_kb = blockIdx.x == 0 ? args.stall_kb : -1;
+      for (int t = cluster; t < args.num_tiles && ok; t += clusters) {
+        int mb, nb;
+        gemm_tile_coords(t, args, mb, nb);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (t == cluster && kb == stall_kb) { ok = false; break; }
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
+          if (rank == 0) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * kPairStageBytes);
+          const uint32_t fb = full0_lead + 8 * stage;
+          tma_load_2d_pair(smem_u32(sA + stage * kPairABytes), &tmA, fb, kb * kGemmBK,
+                           mb * (2 * kPairRows) + rank * kPairRows);
+          tma_load_2d_pair(smem_u32(sB + stage * kPairBBytes), &tmB, fb, kb * kGemmBK,
+                           nb * kGemmBN + rank * kPairRows);
+          if (++stage == kPairStages) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!ok && rank == 0) {
+        // let copies already in flight (this CTA's and the peer's, all
+        // counted here) land before the CTA exits
+        for (int s = 0; s < kPairStages; ++s) mbar_wait_drain(full0 + 8 * s, phase);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (rank 0 of the pair)
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * kPairRows, kGemmBN);
+      const uint32_t a_lo0 = sdesc_lo(smem_u32(sA));
+      const uint32_t b_lo0 = sdesc_lo(smem_u32(sB));
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = cluster; t < args.num_tiles && ok; t += clusters, ++it) {
+        const int acc = it & 1;
+        if (!mbar_wait(tempty0 + 8 * acc, ((it >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kGemmBN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_lo = a_lo0 + stage * (kPairABytes >> 4);
+          const uint32_t b_lo = b_lo0 + stage * (kPairBBytes >> 4);
+#pragma unroll
+          for (int k = 0; k < kGemmBK / 16; ++k)
+            tc_mma_pair_lo(d_tmem, a_lo + 2 * k, b_lo + 2 * k, idesc, (kb | k) != 0);
+          tc_commit_pair(empty0 + 8 * stage, 0x3);
+          if (++stage == kPairStages) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit_pair(tfull0 + 8 * acc, 0x3);
+      }
+      // every MMA issued by this thread has completed once `drain` flips
+      tc_commit_pair(drain, 0x1);
+      mbar_wait_drain(drain, 0);
+    }
+  } else {
+    // ---------------- epilogue warps 2..5 (both CTAs): TMEM lane quarter = warp % 4
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    int it = 0;
+    for (int t = cluster; t < args.num_tiles; t += clusters, ++it) {
+      int mb, nb;
+      gemm_tile_coords(t, args, mb, nb);
+      const int acc = it & 1;
+      if (!mbar_wait(tfull0 + 8 * acc, (it >> 1) & 1, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kGemmBN;
+      const int grow = mb * (2 * kPairRows) + static_cast<int>(rank) * kPairRows + row;
+#pragma unroll 1
+      for (int c = 0; c < kGemmBN / 32; ++c) {
+        float v[32];
+        tmem_ld32(tbase + c * 32, v);
+        gemm_epilogue_chunk<EPI>(args, v, grow, nb * kGemmBN + c * 32);
+      }
+      tc_fence_before();
+      mbar_arrive_cluster(tempty0_lead + 8 * acc);
+    }
+  }
+
+  // neither CTA frees its tensor memory (or exits) while the pair's MMAs or
+  // the other CTA's copies may still touch it
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, kGemmTmemCols);
 }
 
 }  // namespace h3

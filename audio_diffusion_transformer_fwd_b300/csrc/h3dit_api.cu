@@ -301,8 +301,114 @@ h3dit_status gemm_setup(const void* A, const void* B, int M, int N, int K, CUten
   return H3DIT_OK;
 }
 
+// Which BF16 projection kernel runs: the CTA-pair kernel unless
+// H3DIT_GEMM_SINGLE_CTA=1 selects the single-CTA one (an A/B switch, read at
+// every launch; both kernels give the same bits).
+bool gemm_pair_enabled() {
+  const char* e = getenv("H3DIT_GEMM_SINGLE_CTA");
+  return !(e && e[0] && e[0] != '0');
+}
+
+// Clusters of two CTA-pair GEMM CTAs that fit the device at once (the
+// persistent grid's size), per kernel and device.
+template <typename K>
+h3dit_status pair_clusters(K kernel, int* out) {
+  static std::mutex mu;
+  static std::vector<std::pair<std::pair<const void*, int>, int>> cache;
+  int dev = 0;
+  H3_CUDA(cudaGetDevice(&dev));
+  const void* key = reinterpret_cast<const void*>(kernel);
+  std::lock_guard<std::mutex> lk(mu);
+  for (auto& e : cache)
+    if (e.first.first == key && e.first.second == dev) {
+      *out = e.second;
+      return H3DIT_OK;
+    }
+  cudaLaunchConfig_t lc{};
+  lc.gridDim = dim3(2 * (sm_count() / 2));
+  lc.blockDim = dim3(h3::kGemmThreads);
+  lc.dynamicSmemBytes = h3::kPairSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  int n = 0;
+  H3_CUDA(cudaOccupancyMaxActiveClusters(&n, kernel, &lc));
+  if (n < 1) return fail(H3DIT_E_CUDA, "no CTA pair of the projection kernel fits the device");
+  cache.push_back({{key, dev}, n});
+  *out = n;
+  return H3DIT_OK;
+}
+
+template <int EPI>
+h3dit_status launch_pair_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const h3::GemmArgs& args,
+                                cudaStream_t s) {
+  auto kernel = h3::gemm_bf16_pair_kernel<EPI>;
+  H3_TRY(set_smem(kernel, h3::kPairSmemBytes));
+  int fit = 0;
+  H3_TRY(pair_clusters(kernel, &fit));
+  const int clusters = std::min(args.num_tiles, fit);
+  cudaLaunchConfig_t lc{};
+  lc.gridDim = dim3(2 * clusters);
+  lc.blockDim = dim3(h3::kGemmThreads);
+  lc.dynamicSmemBytes = h3::kPairSmemBytes;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  H3_CUDA(cudaLaunchKernelEx(&lc, kernel, ta, tb, args));
+  return H3DIT_OK;
+}
+
+// The projection on CTA pairs: 256 x 256 output tiles, each CTA of a pair
+// loading 128 A rows and 128 of the tile's 256 weight rows per k-block.
+h3dit_status launch_gemm_pair(int epi, const void* A, const void* B, int M, int N, int K, h3::GemmArgs args,
+                              int cls, cudaStream_t s) {
+  if (M < 1 || N % h3::kGemmBN != 0 || K % h3::kGemmBK != 0 || N <= 0 || K <= 0)
+    return fail(H3DIT_E_UNSUPPORTED, "gemm shape %dx%dx%d (n %% 256, k %% 64)", M, N, K);
+  if (!aligned(A, 16) || !aligned(B, 16)) return fail(H3DIT_E_INVAL, "gemm operands must be 16-byte aligned");
+  CUtensorMap ta, tb;
+  {
+    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)M};
+    const uint64_t str[1] = {(uint64_t)K * 2};
+    const uint32_t box[2] = {h3::kGemmBK, h3::kPairRows};
+    H3_TRY(make_map(&ta, A, 2, dims, str, box));
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)N};
+    const uint64_t str[1] = {(uint64_t)K * 2};
+    const uint32_t box[2] = {h3::kGemmBK, h3::kPairRows};
+    H3_TRY(make_map(&tb, B, 2, dims, str, box));
+  }
+  args.M = M;
+  args.N = N;
+  args.K = K;
+  args.tiles_m = (M + 2 * h3::kPairRows - 1) / (2 * h3::kPairRows);
+  args.tiles_n = N / h3::kGemmBN;
+  args.num_tiles = args.tiles_m * args.tiles_n;
+  args.stall_kb = take_stall_request();
+  if (args.stall_kb >= K / h3::kGemmBK) args.stall_kb = -1;
+  TimedLaunch tl(cls, s);
+  switch (epi) {
+    case h3::kEpiStore: H3_TRY(launch_pair_kernel<h3::kEpiStore>(ta, tb, args, s)); break;
+    case h3::kEpiGelu: H3_TRY(launch_pair_kernel<h3::kEpiGelu>(ta, tb, args, s)); break;
+    case h3::kEpiQKV: H3_TRY(launch_pair_kernel<h3::kEpiQKV>(ta, tb, args, s)); break;
+    default: return fail(H3DIT_E_INVAL, "unknown epilogue %d", epi);
+  }
+  H3_CUDA(cudaGetLastError());
+  return H3DIT_OK;
+}
+
 h3dit_status launch_gemm(int epi, const void* A, const void* B, int M, int N, int K, h3::GemmArgs args,
                          int cls, cudaStream_t s) {
+  if (gemm_pair_enabled()) return launch_gemm_pair(epi, A, B, M, N, K, args, cls, s);
   CUtensorMap ta, tb;
   H3_TRY(gemm_setup(A, B, M, N, K, ta, tb, args));
   args.stall_kb = take_stall_request();

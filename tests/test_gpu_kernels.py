@@ -107,14 +107,20 @@ def test_attention(dh, n):
     _close(host(o), ref, rel=1e-2, amax_frac=2.0 ** -6)
 
 
-def test_attention_large_logits_rescale():
+@pytest.mark.parametrize("mixed", [False, True])
+def test_attention_large_logits_rescale(mixed):
     """Keys whose scores grow along the sequence force the running max to be
-    raised (and O rescaled) at every tile."""
+    raised (and O rescaled) at every tile.  ``mixed``: only every other query
+    row sees the growth (the others score every key near 0), so within one
+    warp some rows redo a tile with a new max while the rest keep theirs."""
     heads, dh, n = 1, 128, 1024
     shape = H.BlockShape(heads * dh, heads, dh, 256)
     r = np.random.default_rng(7)
     q = np.zeros((heads, n, dh), np.float32)
     q[..., 0] = 1.0
+    if mixed:
+        q[:, 1::2, 0] = 0.0
+        q[:, 1::2, 1:] = r.standard_normal((heads, n // 2, dh - 1)).astype(np.float32)
     k = r.standard_normal((heads, n, dh)).astype(np.float32) * 0.1
     k[..., 0] = np.linspace(0, 1000, n, dtype=np.float32)   # scaled score rises ~16 (log2) per tile
     q, k = synth.to_bf16_values(q), synth.to_bf16_values(k)
@@ -250,3 +256,26 @@ def test_abi_errors():
     with pytest.raises(H.H3DitError) as e:
         H.h3dit_block_forward(ok, H.block_weights(None, None, None, None), None, None, None, 256, None, 0)
     assert e.value.status == H.E_INVAL
+
+
+@pytest.mark.parametrize("m,n,k,act", [(256, 256, 64, 0), (77, 256, 128, 1), (1, 512, 64, 0), (300, 768, 2048, 1),
+                                       (1000, 512, 1024, 0), (513, 1024, 5120, 1)])
+def test_pair_and_single_cta_projection_agree_bit_for_bit(monkeypatch, m, n, k, act):
+    """The CTA-pair projection kernel (two SMs per 256 x 256 tile) and the
+    single-CTA kernel (one SM per 128 x 256 tile) add the same products in
+    the same order: their outputs are identical, ragged M tails included."""
+    r = np.random.default_rng(m + n + k)
+    a = dev_bf16(r.standard_normal((m, k)).astype(np.float32))
+    b = dev_bf16(r.standard_normal((n, k)).astype(np.float32) * 0.05)
+    out = []
+    for single in ("1", "0"):
+        monkeypatch.setenv("H3DIT_GEMM_SINGLE_CTA", single)
+        c = torch.zeros((m, n), device="cuda", dtype=torch.bfloat16)
+        H.h3dit_linear(a, b, m, n, k, act, c)
+        H.h3dit_check_device_error()
+        out.append(c)
+    assert torch.equal(out[0], out[1])
+    ref = O.bf16_round(host(a) @ host(b).T)
+    if act:
+        ref = O.bf16_round(O.gelu_tanh(host(a) @ host(b).T))
+    assert rel_l2(host(out[1]), ref) <= 5e-3
