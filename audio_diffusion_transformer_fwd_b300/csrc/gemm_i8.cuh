@@ -86,87 +86,118 @@ __device__ __forceinline__ void i8_epilogue16(const GemmArgs& a, const float (&v
   }
 }
 
-template <int EPI, int MODE>
+// PAIR: the same kernel on CTA pairs (tcgen05 cta_group::2), as the BF16
+// projections run (gemm.cuh): 256 x 256 tiles over two SMs, each CTA
+// streaming its 128 A rows and 128 of the 256 weight rows per k-block into
+// a 6-deep ring, rank 0 issuing M = 256 MMAs, each CTA's eight epilogue
+// warps draining its own 128 rows of every chunk.
+template <int EPI, int MODE, bool PAIR>
 __global__ void __launch_bounds__(kI8Threads, 1)
     gemm_i8x_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const GemmArgs args,
                        const I8Args qa) {
+  constexpr int kStages = PAIR ? kPairStages : kGemmStages;
+  constexpr int kABytes = PAIR ? kPairABytes : kGemmABytes;
+  constexpr int kBBytes = PAIR ? kPairBBytes : kGemmBBytes;
+  constexpr int kTileM = PAIR ? 2 * kPairRows : kGemmBM;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + kGemmStages * kGemmABytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kGemmStages * kGemmStageBytes);
+  uint8_t* sB = smem + kStages * kABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * (kABytes + kBBytes));
   // bars: full[S], empty[S], tfull[2], tempty[2], drain
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kGemmStages + 5);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int first = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   const uint32_t full0 = smem_u32(bars);
-  const uint32_t empty0 = smem_u32(bars + kGemmStages);
-  const uint32_t tfull0 = smem_u32(bars + 2 * kGemmStages);
-  const uint32_t tempty0 = smem_u32(bars + 2 * kGemmStages + 2);
-  const uint32_t drain = smem_u32(bars + 2 * kGemmStages + 4);
+  const uint32_t empty0 = smem_u32(bars + kStages);
+  const uint32_t tfull0 = smem_u32(bars + 2 * kStages);
+  const uint32_t tempty0 = smem_u32(bars + 2 * kStages + 2);
+  const uint32_t drain = smem_u32(bars + 2 * kStages + 4);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kGemmStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(tfull0 + 8 * i, 1);
-      mbar_init(tempty0 + 8 * i, 256);
+      mbar_init(tempty0 + 8 * i, PAIR ? 2 * 256 : 256);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_holder), kGemmTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_holder), kGemmTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_holder), kGemmTmemCols);
+      tmem_relinquish();
+    }
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const int kblocks = args.K / kGemmBK;
   const int nchunks = (kblocks + qa.chunk_kb - 1) / qa.chunk_kb;
+  const uint32_t full0_lead = PAIR ? mapa_shared(full0, 0) : full0;
+  const uint32_t tempty0_lead = PAIR ? mapa_shared(tempty0, 0) : tempty0;
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer
+      // ---------------- TMA producer (both CTAs of a pair)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
+      for (int t = first; t < args.num_tiles && ok; t += step) {
         int mb, nb;
         gemm_tile_coords(t, args, mb, nb);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
-          const uint32_t fb = full0 + 8 * stage;
-          mbar_arrive_expect_tx(fb, kGemmStageBytes);
-          tma_load_2d(smem_u32(sA + stage * kGemmABytes), &tmA, fb, kb * kGemmBK, mb * kGemmBM);
-          tma_load_2d(smem_u32(sB + stage * kGemmBBytes), &tmB, fb, kb * kGemmBK, nb * kGemmBN);
-          if (++stage == kGemmStages) { stage = 0; phase ^= 1; }
+          if constexpr (PAIR) {
+            if (rank == 0) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * (kABytes + kBBytes));
+            const uint32_t fb = full0_lead + 8 * stage;
+            tma_load_2d_pair(smem_u32(sA + stage * kABytes), &tmA, fb, kb * kGemmBK,
+                             mb * kTileM + static_cast<int>(rank) * kPairRows);
+            tma_load_2d_pair(smem_u32(sB + stage * kBBytes), &tmB, fb, kb * kGemmBK,
+                             nb * kGemmBN + static_cast<int>(rank) * kPairRows);
+          } else {
+            const uint32_t fb = full0 + 8 * stage;
+            mbar_arrive_expect_tx(fb, kABytes + kBBytes);
+            tma_load_2d(smem_u32(sA + stage * kABytes), &tmA, fb, kb * kGemmBK, mb * kTileM);
+            tma_load_2d(smem_u32(sB + stage * kBBytes), &tmB, fb, kb * kGemmBK, nb * kGemmBN);
+          }
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
-      if (!ok) {
-        for (int s = 0; s < kGemmStages; ++s) mbar_wait_drain(full0 + 8 * s, phase);
+      if (!ok && rank == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_wait_drain(full0 + 8 * s, phase);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       // ---------------- MMA issuer: one accumulator per chunk, alternating
-      constexpr uint32_t idesc = idesc_bf16_f32(kGemmBM, kGemmBN);
+      constexpr uint32_t idesc = idesc_bf16_f32(kTileM, kGemmBN);
+      const uint32_t a_lo0 = sdesc_lo(smem_u32(sA));
+      const uint32_t b_lo0 = sdesc_lo(smem_u32(sB));
       int stage = 0;
       uint32_t phase = 0;
       int cc = 0;   // chunks issued so far by this CTA
       bool ok = true;
-      for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
+      for (int t = first; t < args.num_tiles && ok; t += step) {
         for (int ch = 0; ch < nchunks && ok; ++ch, ++cc) {
           const int acc = cc & 1;
           if (!mbar_wait(tempty0 + 8 * acc, ((cc >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
@@ -177,21 +208,25 @@ __global__ void __launch_bounds__(kI8Threads, 1)
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t a0 = smem_u32(sA + stage * kGemmABytes);
-            const uint32_t b0 = smem_u32(sB + stage * kGemmBBytes);
+            const uint32_t a_lo = a_lo0 + stage * (kABytes >> 4);
+            const uint32_t b_lo = b_lo0 + stage * (kBBytes >> 4);
 #pragma unroll
             for (int k = 0; k < kGemmBK / 16; ++k) {
-              tc_mma_bf16(d_tmem, sdesc_k128(a0 + 32 * k), sdesc_k128(b0 + 32 * k), idesc,
-                          (kb != kb0 || k != 0) ? 1u : 0u);
+              const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
+              if constexpr (PAIR) tc_mma_pair_lo(d_tmem, a_lo + 2 * k, b_lo + 2 * k, idesc, accum);
+              else tc_mma_ss_lo(d_tmem, a_lo + 2 * k, b_lo + 2 * k, idesc, accum);
             }
-            tc_commit(empty0 + 8 * stage);
-            if (++stage == kGemmStages) { stage = 0; phase ^= 1; }
+            if constexpr (PAIR) tc_commit_pair(empty0 + 8 * stage, 0x3);
+            else tc_commit(empty0 + 8 * stage);
+            if (++stage == kStages) { stage = 0; phase ^= 1; }
           }
           if (!ok) break;
-          tc_commit(tfull0 + 8 * acc);
+          if constexpr (PAIR) tc_commit_pair(tfull0 + 8 * acc, 0x3);
+          else tc_commit(tfull0 + 8 * acc);
         }
       }
-      tc_commit(drain);
+      if constexpr (PAIR) tc_commit_pair(drain, 0x1);
+      else tc_commit(drain);
       mbar_wait_drain(drain, 0);
     }
   } else {
@@ -201,10 +236,10 @@ __global__ void __launch_bounds__(kI8Threads, 1)
     const int row = quarter * 32 + lane;
     int cc = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
+    for (int t = first; t < args.num_tiles && ok; t += step) {
       int mb, nb;
       gemm_tile_coords(t, args, mb, nb);
-      const int grow = mb * kGemmBM + row;
+      const int grow = mb * kTileM + static_cast<int>(rank) * kPairRows * (PAIR ? 1 : 0) + row;
       const bool live = grow < args.M;
       const int col0 = nb * kGemmBN + half * 128;
       int iacc[128];
@@ -238,7 +273,8 @@ __global__ void __launch_bounds__(kI8Threads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(tempty0 + 8 * acc);
+        if constexpr (PAIR) mbar_arrive_cluster(tempty0_lead + 8 * acc);
+        else mbar_arrive(tempty0 + 8 * acc);
       }
       if (!ok) break;
       if (!live) continue;
@@ -276,9 +312,13 @@ __global__ void __launch_bounds__(kI8Threads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();
+  else __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, kGemmTmemCols);
+  if (warp == 1) {
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, kGemmTmemCols);
+    else tmem_dealloc(tmem_base, kGemmTmemCols);
+  }
 }
 
 }  // namespace h3

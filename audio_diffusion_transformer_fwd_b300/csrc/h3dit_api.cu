@@ -39,12 +39,16 @@ h3dit_status fail(h3dit_status st, const char* fmt, ...) {
   return st;
 }
 
+// A failed runtime call is reported and then cleared from the runtime's
+// last-error slot, so that it does not resurface at the next call's check.
 #define H3_CUDA(call)                                                                 \
   do {                                                                                \
     cudaError_t e_ = (call);                                                          \
-    if (e_ != cudaSuccess)                                                            \
+    if (e_ != cudaSuccess) {                                                          \
+      cudaGetLastError();                                                             \
       return fail(H3DIT_E_CUDA, "%s: %s (%s:%d)", #call, cudaGetErrorString(e_),     \
                   __FILE__, __LINE__);                                                \
+    }                                                                                 \
   } while (0)
 
 #define H3_TRY(expr)                       \
@@ -312,7 +316,7 @@ bool gemm_pair_enabled() {
 // Clusters of two CTA-pair GEMM CTAs that fit the device at once (the
 // persistent grid's size), per kernel and device.
 template <typename K>
-h3dit_status pair_clusters(K kernel, int* out) {
+h3dit_status pair_clusters(K kernel, int threads, size_t smem_bytes, int* out) {
   static std::mutex mu;
   static std::vector<std::pair<std::pair<const void*, int>, int>> cache;
   int dev = 0;
@@ -326,8 +330,8 @@ h3dit_status pair_clusters(K kernel, int* out) {
     }
   cudaLaunchConfig_t lc{};
   lc.gridDim = dim3(2 * (sm_count() / 2));
-  lc.blockDim = dim3(h3::kGemmThreads);
-  lc.dynamicSmemBytes = h3::kPairSmemBytes;
+  lc.blockDim = dim3(threads);
+  lc.dynamicSmemBytes = smem_bytes;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -343,18 +347,19 @@ h3dit_status pair_clusters(K kernel, int* out) {
   return H3DIT_OK;
 }
 
-template <int EPI>
-h3dit_status launch_pair_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const h3::GemmArgs& args,
-                                cudaStream_t s) {
-  auto kernel = h3::gemm_bf16_pair_kernel<EPI>;
-  H3_TRY(set_smem(kernel, h3::kPairSmemBytes));
+// A persistent kernel on CTA pairs: as many clusters of two as fit the
+// device at once (at most one per tile), each walking tiles cluster,
+// cluster + clusters, ...
+template <typename K, typename... A>
+h3dit_status launch_on_pairs(K kernel, int threads, size_t smem_bytes, int tiles, cudaStream_t s, A... args) {
+  H3_TRY(set_smem(kernel, smem_bytes));
   int fit = 0;
-  H3_TRY(pair_clusters(kernel, &fit));
-  const int clusters = std::min(args.num_tiles, fit);
+  H3_TRY(pair_clusters(kernel, threads, smem_bytes, &fit));
+  const int clusters = std::min(tiles, fit);
   cudaLaunchConfig_t lc{};
   lc.gridDim = dim3(2 * clusters);
-  lc.blockDim = dim3(h3::kGemmThreads);
-  lc.dynamicSmemBytes = h3::kPairSmemBytes;
+  lc.blockDim = dim3(threads);
+  lc.dynamicSmemBytes = smem_bytes;
   lc.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -363,18 +368,25 @@ h3dit_status launch_pair_kernel(const CUtensorMap& ta, const CUtensorMap& tb, co
   attr[0].val.clusterDim.z = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  H3_CUDA(cudaLaunchKernelEx(&lc, kernel, ta, tb, args));
+  H3_CUDA(cudaLaunchKernelEx(&lc, kernel, args...));
   return H3DIT_OK;
 }
 
-// The projection on CTA pairs: 256 x 256 output tiles, each CTA of a pair
-// loading 128 A rows and 128 of the tile's 256 weight rows per k-block.
-h3dit_status launch_gemm_pair(int epi, const void* A, const void* B, int M, int N, int K, h3::GemmArgs args,
-                              int cls, cudaStream_t s) {
+template <int EPI>
+h3dit_status launch_pair_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const h3::GemmArgs& args,
+                                cudaStream_t s) {
+  return launch_on_pairs(h3::gemm_bf16_pair_kernel<EPI>, h3::kGemmThreads, h3::kPairSmemBytes, args.num_tiles, s,
+                         ta, tb, args);
+}
+
+// Tensor maps and tile counts of a projection on CTA pairs: 256 x 256
+// output tiles, each CTA of a pair loading 128 A rows and 128 of the tile's
+// 256 weight rows per k-block.
+h3dit_status pair_setup(const void* A, const void* B, int M, int N, int K, CUtensorMap& ta, CUtensorMap& tb,
+                        h3::GemmArgs& args) {
   if (M < 1 || N % h3::kGemmBN != 0 || K % h3::kGemmBK != 0 || N <= 0 || K <= 0)
     return fail(H3DIT_E_UNSUPPORTED, "gemm shape %dx%dx%d (n %% 256, k %% 64)", M, N, K);
   if (!aligned(A, 16) || !aligned(B, 16)) return fail(H3DIT_E_INVAL, "gemm operands must be 16-byte aligned");
-  CUtensorMap ta, tb;
   {
     const uint64_t dims[2] = {(uint64_t)K, (uint64_t)M};
     const uint64_t str[1] = {(uint64_t)K * 2};
@@ -390,9 +402,17 @@ h3dit_status launch_gemm_pair(int epi, const void* A, const void* B, int M, int 
   args.M = M;
   args.N = N;
   args.K = K;
+  args.stall_kb = -1;
   args.tiles_m = (M + 2 * h3::kPairRows - 1) / (2 * h3::kPairRows);
   args.tiles_n = N / h3::kGemmBN;
   args.num_tiles = args.tiles_m * args.tiles_n;
+  return H3DIT_OK;
+}
+
+h3dit_status launch_gemm_pair(int epi, const void* A, const void* B, int M, int N, int K, h3::GemmArgs args,
+                              int cls, cudaStream_t s) {
+  CUtensorMap ta, tb;
+  H3_TRY(pair_setup(A, B, M, N, K, ta, tb, args));
   args.stall_kb = take_stall_request();
   if (args.stall_kb >= K / h3::kGemmBK) args.stall_kb = -1;
   TimedLaunch tl(cls, s);
@@ -440,9 +460,15 @@ h3dit_status launch_gemm(int epi, const void* A, const void* B, int M, int N, in
 
 template <int EPI, int MODE>
 h3dit_status launch_i8_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const h3::GemmArgs& args,
-                              const h3::I8Args& qa, int grid, cudaStream_t s) {
-  H3_TRY(set_smem(h3::gemm_i8x_tc_kernel<EPI, MODE>, h3::kGemmSmemBytes));
-  h3::gemm_i8x_tc_kernel<EPI, MODE><<<grid, h3::kI8Threads, h3::kGemmSmemBytes, s>>>(ta, tb, args, qa);
+                              const h3::I8Args& qa, bool pair, cudaStream_t s) {
+  if (pair) {
+    H3_TRY(launch_on_pairs(h3::gemm_i8x_tc_kernel<EPI, MODE, true>, h3::kI8Threads, h3::kPairSmemBytes,
+                           args.num_tiles, s, ta, tb, args, qa));
+  } else {
+    const int grid = std::min(args.num_tiles, sm_count());
+    H3_TRY(set_smem(h3::gemm_i8x_tc_kernel<EPI, MODE, false>, h3::kGemmSmemBytes));
+    h3::gemm_i8x_tc_kernel<EPI, MODE, false><<<grid, h3::kI8Threads, h3::kGemmSmemBytes, s>>>(ta, tb, args, qa);
+  }
   H3_CUDA(cudaGetLastError());
   return H3DIT_OK;
 }
@@ -454,7 +480,9 @@ h3dit_status launch_i8_kernel(const CUtensorMap& ta, const CUtensorMap& tb, cons
 h3dit_status launch_gemm_i8(int epi, const void* A, const float* sa, int group, const void* B, const float* sb,
                             int M, int N, int K, h3::GemmArgs args, int32_t* acc, int cls, cudaStream_t s) {
   CUtensorMap ta, tb;
-  H3_TRY(gemm_setup(A, B, M, N, K, ta, tb, args));
+  const bool pair = gemm_pair_enabled();
+  if (pair) H3_TRY(pair_setup(A, B, M, N, K, ta, tb, args));
+  else H3_TRY(gemm_setup(A, B, M, N, K, ta, tb, args));
   if (K > (1 << 17)) return fail(H3DIT_E_UNSUPPORTED, "int8 k %d (the int32 accumulator bound needs k <= 131072)", K);
   h3::I8Args qa{};
   qa.sa = sa;
@@ -473,20 +501,19 @@ h3dit_status launch_gemm_i8(int epi, const void* A, const float* sa, int group, 
   }
   if (epi != h3::kEpiAcc && (!sa || !sb || !aligned(sb, 16)))
     return fail(H3DIT_E_INVAL, "int8 scales missing or sb not 16-byte aligned");
-  const int grid = std::min(args.num_tiles, sm_count());
   TimedLaunch tl(cls, s);
   if (grouped) {
     switch (epi) {
-      case h3::kEpiStore: return launch_i8_kernel<h3::kEpiStore, h3::kI8Group>(ta, tb, args, qa, grid, s);
-      case h3::kEpiGelu: return launch_i8_kernel<h3::kEpiGelu, h3::kI8Group>(ta, tb, args, qa, grid, s);
+      case h3::kEpiStore: return launch_i8_kernel<h3::kEpiStore, h3::kI8Group>(ta, tb, args, qa, pair, s);
+      case h3::kEpiGelu: return launch_i8_kernel<h3::kEpiGelu, h3::kI8Group>(ta, tb, args, qa, pair, s);
       default: return fail(H3DIT_E_INVAL, "grouped int8 epilogue %d", epi);
     }
   }
   switch (epi) {
-    case h3::kEpiStore: return launch_i8_kernel<h3::kEpiStore, h3::kI8Int>(ta, tb, args, qa, grid, s);
-    case h3::kEpiGelu: return launch_i8_kernel<h3::kEpiGelu, h3::kI8Int>(ta, tb, args, qa, grid, s);
-    case h3::kEpiQKV: return launch_i8_kernel<h3::kEpiQKV, h3::kI8Int>(ta, tb, args, qa, grid, s);
-    case h3::kEpiAcc: return launch_i8_kernel<h3::kEpiAcc, h3::kI8Int>(ta, tb, args, qa, grid, s);
+    case h3::kEpiStore: return launch_i8_kernel<h3::kEpiStore, h3::kI8Int>(ta, tb, args, qa, pair, s);
+    case h3::kEpiGelu: return launch_i8_kernel<h3::kEpiGelu, h3::kI8Int>(ta, tb, args, qa, pair, s);
+    case h3::kEpiQKV: return launch_i8_kernel<h3::kEpiQKV, h3::kI8Int>(ta, tb, args, qa, pair, s);
+    case h3::kEpiAcc: return launch_i8_kernel<h3::kEpiAcc, h3::kI8Int>(ta, tb, args, qa, pair, s);
     default: return fail(H3DIT_E_INVAL, "int8 epilogue %d", epi);
   }
 }
