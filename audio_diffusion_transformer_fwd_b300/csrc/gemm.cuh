@@ -36,7 +36,7 @@ constexpr int kGemmABytes = kGemmBM * kGemmBK * 2;   // 16 KB
 constexpr int kGemmBBytes = kGemmBN * kGemmBK * 2;   // 32 KB
 constexpr int kGemmStageBytes = kGemmABytes + kGemmBBytes;
 constexpr int kGemmTmemCols = 2 * kGemmBN;           // two accumulators
-constexpr int kGemmGroupN = 16;                      // tile raster: bands of 16 N-tiles
+constexpr int kGemmGroupN = 16;                      // default tile raster: bands of 16 N-tiles
 constexpr size_t kGemmSmemBytes = 1024 /*align slack*/ + kGemmStages * kGemmStageBytes + 256;
 
 struct GemmArgs {
@@ -56,6 +56,7 @@ struct GemmArgs {
   // k-block `stall_kb` of its first tile and issues nothing more, so the MMA
   // thread's wait on that stage runs out (see h3dit_test_stall_next_gemm).
   int stall_kb;
+  int band_n;   // tile raster: output tiles are walked in bands of band_n N-tiles, M fastest within a band
 };
 
 __device__ __forceinline__ float gelu_tanh_f(float x) {
@@ -65,11 +66,11 @@ __device__ __forceinline__ float gelu_tanh_f(float x) {
 }
 
 __device__ __forceinline__ void gemm_tile_coords(int t, const GemmArgs& a, int& mb, int& nb) {
-  const int per_group = kGemmGroupN * a.tiles_m;
+  const int per_group = a.band_n * a.tiles_m;
   const int g = t / per_group;
   const int r = t - g * per_group;
-  const int n_first = g * kGemmGroupN;
-  const int gn = min(kGemmGroupN, a.tiles_n - n_first);
+  const int n_first = g * a.band_n;
+  const int gn = min(a.band_n, a.tiles_n - n_first);
   mb = r / gn;
   nb = n_first + (r - mb * gn);
 }

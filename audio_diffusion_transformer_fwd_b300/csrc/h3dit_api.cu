@@ -278,6 +278,14 @@ h3dit_status set_smem(K kernel, size_t bytes) {
 
 // Tensor maps of the GEMM operands A [M][K] and B [N][K] (BF16, K-major) and
 // the tile counts; shared by the BF16 and the int8-code kernels.
+// Width of the projections' tile raster in N-tiles: 16 unless H3DIT_GEMM_BAND
+// names another width (1..64; a tuning switch, read at every launch).
+int gemm_band() {
+  const char* e = getenv("H3DIT_GEMM_BAND");
+  const int v = e ? atoi(e) : 0;
+  return (v >= 1 && v <= 64) ? v : h3::kGemmGroupN;
+}
+
 h3dit_status gemm_setup(const void* A, const void* B, int M, int N, int K, CUtensorMap& ta, CUtensorMap& tb,
                         h3::GemmArgs& args) {
   if (M < 1 || N % h3::kGemmBN != 0 || K % h3::kGemmBK != 0 || N <= 0 || K <= 0)
@@ -299,6 +307,7 @@ h3dit_status gemm_setup(const void* A, const void* B, int M, int N, int K, CUten
   args.N = N;
   args.K = K;
   args.stall_kb = -1;
+  args.band_n = gemm_band();
   args.tiles_m = (M + h3::kGemmBM - 1) / h3::kGemmBM;
   args.tiles_n = N / h3::kGemmBN;
   args.num_tiles = args.tiles_m * args.tiles_n;
@@ -403,6 +412,7 @@ h3dit_status pair_setup(const void* A, const void* B, int M, int N, int K, CUten
   args.N = N;
   args.K = K;
   args.stall_kb = -1;
+  args.band_n = gemm_band();
   args.tiles_m = (M + 2 * h3::kPairRows - 1) / (2 * h3::kPairRows);
   args.tiles_n = N / h3::kGemmBN;
   args.num_tiles = args.tiles_m * args.tiles_n;
