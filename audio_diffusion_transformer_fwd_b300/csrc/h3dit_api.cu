@@ -680,6 +680,7 @@ struct Arena {
   size_t a1 = 0, a2 = 0, a3 = 0, rope = 0;     // offsets
   size_t xred = 0, rope_red = 0, pos_red = 0;  // reduction extras
   size_t sc_row = 0, sc_grp = 0;               // int8 activation scales
+  size_t widen = 0;                            // int8 weights given as bytes: one projection's operand form
   size_t total = 0;
   int vt_ld = 0;
 };
@@ -714,6 +715,12 @@ Arena plan_arena(const h3dit_config* c, int n, const h3dit_reduction* tr) {
   if (int8_set(c->precision).any()) {
     a.sc_row = off; off += round_up((size_t)n * 4, 256);
     a.sc_grp = off; off += round_up((size_t)n * (F / fc2_group(c)) * 4, 256);
+    const Int8Set q8 = int8_set(c->precision);
+    size_t wmax = 0;
+    if (q8.qkv) wmax = std::max(wmax, 3 * d * d);
+    if (q8.o) wmax = std::max(wmax, d * d);
+    if (q8.fc1 || q8.fc2) wmax = std::max(wmax, F * d);
+    a.widen = off; off += round_up(wmax * 2, 256);
   }
   if (tr) {
     const h3::PairGrid g = pair_grid(&tr->grid, n);
@@ -749,6 +756,19 @@ h3dit_status run_block_body(const h3dit_config* c, const h3dit_block_weights* w,
   bf16* a3 = reinterpret_cast<bf16*>(B.base + B.ar.a3);
   float* sc_row = q8.any() ? reinterpret_cast<float*>(B.base + B.ar.sc_row) : nullptr;
   float* sc_grp = q8.any() ? reinterpret_cast<float*>(B.base + B.ar.sc_grp) : nullptr;
+  // int8 weights given as bytes are widened into this slot just before
+  // their projection (every projection is done with it before the next)
+  bf16* slot = q8.any() ? reinterpret_cast<bf16*>(B.base + B.ar.widen) : nullptr;
+  auto weight = [&](const void* wq, size_t count, const void** out) -> h3dit_status {
+    *out = wq;
+    if (!w->codes_int8) return H3DIT_OK;
+    TimedLaunch tl(kQuant, s);
+    const size_t n8 = count / 8;
+    h3::widen_codes_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, s>>>(static_cast<const int8_t*>(wq), n8, slot);
+    H3_CUDA(cudaGetLastError());
+    *out = slot;
+    return H3DIT_OK;
+  };
   bf16* q = reinterpret_cast<bf16*>(a1);
   bf16* k = reinterpret_cast<bf16*>(a1 + round_up((size_t)n * d * 2, 256));
   bf16* vt = reinterpret_cast<bf16*>(a1 + 2 * round_up((size_t)n * d * 2, 256));
@@ -761,9 +781,11 @@ h3dit_status run_block_body(const h3dit_config* c, const h3dit_block_weights* w,
   h3::GemmArgs g{};
   g.q = q; g.k = k; g.vt = vt; g.vt_ld = vt_ld; g.d = d; g.head_dim = dh;
   g.rope = reinterpret_cast<const float2*>(rope);
-  if (q8.qkv)
-    H3_TRY(launch_gemm_i8(h3::kEpiQKV, a2, sc_row, d, w->w_qkv, w->s_qkv, n, 3 * d, d, g, nullptr, kQKV, s));
-  else
+  if (q8.qkv) {
+    const void* wq;
+    H3_TRY(weight(w->w_qkv, (size_t)3 * d * d, &wq));
+    H3_TRY(launch_gemm_i8(h3::kEpiQKV, a2, sc_row, d, wq, w->s_qkv, n, 3 * d, d, g, nullptr, kQKV, s));
+  } else
     H3_TRY(launch_gemm(h3::kEpiQKV, a2, w->w_qkv, n, 3 * d, d, g, kQKV, s));
   h3::GemmArgs go{};
   go.c = a3; go.ldc = d;
@@ -771,7 +793,9 @@ h3dit_status run_block_body(const h3dit_config* c, const h3dit_block_weights* w,
     // o into a3, its codes into a2 (h is dead), the projection back into a3
     H3_TRY(launch_attention(c, q, k, vt, vt_ld, n, a3, s));
     H3_TRY(launch_quantize_codes(a3, n, d, d, a2, sc_row, s));
-    H3_TRY(launch_gemm_i8(h3::kEpiStore, a2, sc_row, d, w->w_o, w->s_o, n, d, d, go, nullptr, kOProj, s));
+    const void* wq;
+    H3_TRY(weight(w->w_o, (size_t)d * d, &wq));
+    H3_TRY(launch_gemm_i8(h3::kEpiStore, a2, sc_row, d, wq, w->s_o, n, d, d, go, nullptr, kOProj, s));
   } else {
     H3_TRY(launch_attention(c, q, k, vt, vt_ld, n, a2, s));
     H3_TRY(launch_gemm(h3::kEpiStore, a2, w->w_o, n, d, d, go, kOProj, s));
@@ -779,15 +803,19 @@ h3dit_status run_block_body(const h3dit_config* c, const h3dit_block_weights* w,
   H3_TRY(launch_rows(x, a3, gate1, shift2, scale2, a2, q8.fc1 ? sc_row : nullptr, n, d, c->eps, s, sm));
   h3::GemmArgs g1{};
   g1.c = u; g1.ldc = F;
-  if (q8.fc1)
-    H3_TRY(launch_gemm_i8(h3::kEpiGelu, a2, sc_row, d, w->w1, w->s1, n, F, d, g1, nullptr, kFC1, s));
-  else
+  if (q8.fc1) {
+    const void* wq;
+    H3_TRY(weight(w->w1, (size_t)F * d, &wq));
+    H3_TRY(launch_gemm_i8(h3::kEpiGelu, a2, sc_row, d, wq, w->s1, n, F, d, g1, nullptr, kFC1, s));
+  } else
     H3_TRY(launch_gemm(h3::kEpiGelu, a2, w->w1, n, F, d, g1, kFC1, s));
   h3::GemmArgs gm{};
   gm.c = a3; gm.ldc = d;
   if (q8.fc2) {
     H3_TRY(launch_quantize_codes(u, n, F, g2, u, sc_grp, s));
-    H3_TRY(launch_gemm_i8(h3::kEpiStore, u, sc_grp, g2, w->w2, w->s2, n, d, F, gm, nullptr, kFC2, s));
+    const void* wq;
+    H3_TRY(weight(w->w2, (size_t)d * F, &wq));
+    H3_TRY(launch_gemm_i8(h3::kEpiStore, u, sc_grp, g2, wq, w->s2, n, d, F, gm, nullptr, kFC2, s));
   } else {
     H3_TRY(launch_gemm(h3::kEpiStore, u, w->w2, n, d, F, gm, kFC2, s));
   }
@@ -836,6 +864,10 @@ h3dit_status check_weights(const h3dit_config* c, const h3dit_block_weights* w) 
   const Int8Set q8 = int8_set(c->precision);
   if ((q8.qkv && !w->s_qkv) || (q8.o && !w->s_o) || (q8.fc1 && !w->s1) || (q8.fc2 && !w->s2))
     return fail(H3DIT_E_INVAL, "an int8 projection needs its weight scales");
+  if (w->codes_int8 != 0 && w->codes_int8 != 1) return fail(H3DIT_E_INVAL, "codes_int8 %d (0 or 1)", w->codes_int8);
+  if (w->codes_int8 && ((q8.qkv && !aligned(w->w_qkv, 8)) || (q8.o && !aligned(w->w_o, 8)) ||
+                        (q8.fc1 && !aligned(w->w1, 8)) || (q8.fc2 && !aligned(w->w2, 8))))
+    return fail(H3DIT_E_INVAL, "int8 weight bytes must be 8-byte aligned");
   return H3DIT_OK;
 }
 

@@ -54,7 +54,7 @@ class Config(ctypes.Structure):
 class BlockWeights(ctypes.Structure):
     _fields_ = [("w_qkv", ctypes.c_void_p), ("w_o", ctypes.c_void_p), ("w1", ctypes.c_void_p),
                 ("w2", ctypes.c_void_p), ("s_qkv", ctypes.c_void_p), ("s_o", ctypes.c_void_p),
-                ("s1", ctypes.c_void_p), ("s2", ctypes.c_void_p)]
+                ("s1", ctypes.c_void_p), ("s2", ctypes.c_void_p), ("codes_int8", ctypes.c_int)]
 
 
 class VideoGrid(ctypes.Structure):
@@ -179,10 +179,11 @@ class BlockShape:
         return c
 
 
-def block_weights(w_qkv, w_o, w1, w2, s_qkv=None, s_o=None, s1=None, s2=None) -> BlockWeights:
+def block_weights(w_qkv, w_o, w1, w2, s_qkv=None, s_o=None, s1=None, s2=None, codes_int8=False) -> BlockWeights:
     bw = BlockWeights()
     bw.w_qkv, bw.w_o, bw.w1, bw.w2 = _ptr(w_qkv), _ptr(w_o), _ptr(w1), _ptr(w2)
     bw.s_qkv, bw.s_o, bw.s1, bw.s2 = _ptr(s_qkv), _ptr(s_o), _ptr(s1), _ptr(s2)
+    bw.codes_int8 = 1 if codes_int8 else 0
     return bw
 
 

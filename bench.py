@@ -549,17 +549,19 @@ def run_int8_block(args, H, synth, torch, stream, barrier, max_over_ranks, rank,
     once, outside the timed region; each variant is timed like the BF16 block."""
     w = synth.WORKLOADS["block_512_int8"]
     n, d, f = w.n_tokens, w.d, w.ffn
-    codes, scales = {}, {}
+    codes, scales, bytes8 = {}, {}, {}
     for k, t in wdev.items():
         q8 = torch.empty(t.shape, device="cuda", dtype=torch.int8)
         sc = torch.empty(t.shape[0], device="cuda", dtype=torch.float32)
         H.h3dit_quantize_weight(t, t.shape[0], t.shape[1], q8, sc, stream)
         cb = torch.empty(t.shape, device="cuda", dtype=torch.bfloat16)
         H.h3dit_widen_codes(q8, q8.numel(), cb, stream)
-        codes[k], scales[k] = cb, sc
-        del q8
+        codes[k], scales[k], bytes8[k] = cb, sc, q8
     names = ("w_qkv", "w_o", "w1", "w2")
-    variants = (("int8", H.INT8, names), ("int8_mlp", H.INT8_MLP, ("w1", "w2")), ("int8_qkv", H.INT8_QKV, ("w_qkv",)))
+    # int8_resident: the same block with the weights kept as int8 bytes,
+    # widened into the workspace before each projection
+    variants = (("int8", H.INT8, names), ("int8_mlp", H.INT8_MLP, ("w1", "w2")), ("int8_qkv", H.INT8_QKV, ("w_qkv",)),
+                ("int8_resident", H.INT8, names))
     burst, sustained, _, peak_src = measured_peaks()
     gops = gemm_flops(n, d, f)
     res = {"workload": "block_512_int8: the block_512 shapes with int8 QKV/out-proj/FC1/FC2 (per-token activation "
@@ -569,9 +571,12 @@ def run_int8_block(args, H, synth, torch, stream, barrier, max_over_ranks, rank,
                         f"peaks = {peak_src} bf16 sustained {sustained} / burst {burst}"}
     for name, prec, q_names in variants:
         shape = H.BlockShape(w.d, w.heads, w.head_dim, w.ffn, w.eps, w.sections, w.theta, prec)
-        ptr = [codes[k] if k in q_names else wdev[k] for k in names]
+        as_bytes = name == "int8_resident"
+        src = bytes8 if as_bytes else codes
+        ptr = [src[k] if k in q_names else wdev[k] for k in names]
         sc = [scales[k] if k in q_names else None for k in names]
-        bw = H.block_weights(*ptr, *sc)
+        bw = H.block_weights(*ptr, *sc, codes_int8=as_bytes)
+        weight_bytes = sum(p.numel() * p.element_size() for p in ptr) + sum(x.numel() * 4 for x in sc if x is not None)
         nbytes = H.h3dit_workspace_size(shape, n)
         wsb = torch.empty(nbytes, device="cuda", dtype=torch.uint8)
         x8 = x.clone()
@@ -604,9 +609,13 @@ def run_int8_block(args, H, synth, torch, stream, barrier, max_over_ranks, rank,
                      "gemm_frac_of_bf16_sustained": gops / (gemm_ms * 1e-3) / 1e12 / sustained,
                      "gemm_frac_of_bf16_burst": gops / (gemm_ms * 1e-3) / 1e12 / burst,
                      "quant_ms": cls["quant"][0] / steps, "rows_ms": cls["rows"][0] / steps,
-                     "attention_ms": cls["attention"][0] / steps, "steps": steps}
+                     "attention_ms": cls["attention"][0] / steps, "steps": steps,
+                     "weight_bytes_resident": weight_bytes}
+        if as_bytes:
+            res[name]["note"] = ("weights kept as int8 bytes (half the operand form) and widened into the "
+                                 "workspace before each projection; quant_ms includes the widening")
         del wsb
-    del codes
+    del codes, bytes8
     torch.cuda.empty_cache()
     return res
 

@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define H3DIT_VERSION 1
+#define H3DIT_VERSION 2
 
 typedef enum {
   H3DIT_OK = 0,
@@ -97,7 +97,14 @@ typedef struct {
  *   w_qkv [3d][d]  rows 0..d-1 give Q (head h = rows h*Dh..), d..2d-1 K, 2d..3d-1 V
  *   w_o   [d][d]   attention output projection
  *   w1    [F][d]   MLP FC1
- *   w2    [d][F]   MLP FC2 */
+ *   w2    [d][F]   MLP FC2
+ * codes_int8 = 1 keeps the int8 projections' weights as plain int8 codes
+ *   (one byte each, 8-byte aligned: half the bytes of the operand form, the
+ *   resident-memory saving of [linlog] "int8 量化"); the library widens each
+ *   into the workspace just before its projection (h3dit_widen_codes'
+ *   rule, so the results equal the operand-form ones bit for bit), at the
+ *   cost of one HBM pass over the operand form per projection and block.
+ *   0 = the operand form above.  BF16 projections ignore it. */
 typedef struct {
   const void* w_qkv;
   const void* w_o;
@@ -107,6 +114,7 @@ typedef struct {
   const float* s_o;
   const float* s1;
   const float* s2;
+  int codes_int8;
 } h3dit_block_weights;
 
 /* Target-video tokens: T*Hh*W consecutive rows starting at row `offset`,
@@ -198,7 +206,9 @@ h3dit_status h3dit_timing_read(int kernel_class, double* total_ms, long long* la
 /* ---------------------------------------------------------------- the block and the step */
 
 /* Bytes of device workspace a block or step at n_tokens needs (tr may be
- * NULL; with a reduction the reduced stream's buffers are included). */
+ * NULL; with a reduction the reduced stream's buffers are included; with an
+ * int8 precision, room for the largest int8 weight in operand form, used
+ * when the weights are given as int8 bytes). */
 h3dit_status h3dit_workspace_size(const h3dit_config* cfg, int n_tokens,
                                   const h3dit_reduction* tr, size_t* bytes);
 

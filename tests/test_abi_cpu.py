@@ -38,7 +38,7 @@ def test_binding_covers_the_header():
 
 def test_host_only_calls(lib):
     lib.h3dit_version.restype = ctypes.c_int
-    assert lib.h3dit_version() == 1
+    assert lib.h3dit_version() == 2
     g = H.video_grid(0, 6, 30, 54)
     assert H.lib().h3dit_reduced_tokens(10488, ctypes.byref(g)) == 5628
     bad = H.video_grid(0, 6, 30, 54)
@@ -118,3 +118,22 @@ def test_stall_request_arguments(lib):
         H.h3dit_test_stall_next_gemm(-2)
     assert e.value.status == H.E_INVAL
     H.h3dit_test_stall_next_gemm(-1)
+
+
+def test_int8_weight_bytes_checked_on_host(lib):
+    """codes_int8 must be 0 or 1, and int8 weight bytes 8-byte aligned; both
+    are refused before anything is enqueued."""
+    shape = H.BlockShape(256, 4, 64, 1024, 1e-6, (16, 24, 24), precision=H.INT8)
+    fake = 1 << 20
+    n = 256
+    need = H.h3dit_workspace_size(shape, n)
+    assert need > H.h3dit_workspace_size(H.BlockShape(256, 4, 64, 1024, 1e-6, (16, 24, 24)), n)
+    bad = H.block_weights(fake + 4, fake, fake, fake, fake, fake, fake, fake, codes_int8=True)
+    with pytest.raises(H.H3DitError) as e:
+        H.h3dit_block_forward(shape, bad, fake, fake, fake, n, fake, need, stream=0)
+    assert e.value.status == H.E_INVAL and "aligned" in str(e.value)
+    odd = H.block_weights(fake, fake, fake, fake, fake, fake, fake, fake)
+    odd.codes_int8 = 2
+    with pytest.raises(H.H3DitError) as e:
+        H.h3dit_block_forward(shape, odd, fake, fake, fake, n, fake, need, stream=0)
+    assert e.value.status == H.E_INVAL and "codes_int8" in str(e.value)

@@ -449,3 +449,52 @@ def test_int8_step_with_token_reduction():
     ref_bf = O.step_forward(x, [p[0] for p in packs], list(mods), pos, cfg, reduction=red, bf16_storage=True,
                             int8=True)
     assert rel_l2(got, ref_bf) <= 1e-2 * nb and rel_l2(got - x, ref_bf - x) <= 2e-2 * nb
+
+
+def test_int8_weights_as_bytes_equal_operand_form():
+    """codes_int8 = 1: the int8 projections' weights stay plain int8 bytes
+    (half the resident bytes) and are widened into the workspace before each
+    projection; the block and a reduced step give the operand-form results
+    bit for bit, for all four projections in int8 and for the MLP alone."""
+    w = TINY
+    n = w.n_tokens
+    pos = dev_f32(synth.positions(w.video, w.n_text, w.n_audio))
+    nb = 5
+    wts = [synth.host_block_weights(w.d, w.ffn, seed=40, block=b) for b in range(nb)]
+    mods = dev_f32(np.stack([synth.host_mod(w.d, seed=40, block=b) for b in range(nb)]))
+    x = synth.host_activations(n, w.d, seed=40)
+    keep, forms = [], {False: [], True: []}
+    for wt in wts:
+        dev16, dev8 = {}, {}
+        for name, qn, sn in (("w_qkv", "q_qkv", "s_qkv"), ("w_o", "q_o", "s_o"), ("w1", "q1", "s1"),
+                             ("w2", "q2", "s2")):
+            q, s = O.quantize_weight(wt[name])
+            dev16[qn], dev8[qn] = codes_dev(q), torch.from_numpy(q).to("cuda")
+            dev16[sn] = dev8[sn] = dev_f32(s[:, 0])
+            dev16[name] = dev8[name] = dev_bf16(wt[name])
+        keep += [dev16, dev8]
+        for as_bytes, dv in ((False, dev16), (True, dev8)):
+            forms[as_bytes].append((dv, as_bytes))
+    T, Hh, W = w.video
+    tr = H.reduction(H.video_grid(0, T, Hh, W), 1, 3)
+    for prec in (H.INT8, H.INT8_MLP):
+        shape = shape_of(w, prec)
+        outs = {}
+        for as_bytes in (False, True):
+            bws = []
+            for dv, ab in forms[as_bytes]:
+                pick = lambda name, qn: dv[qn] if (prec == H.INT8 or name in ("w1", "w2")) else dv[name]
+                bws.append(H.block_weights(pick("w_qkv", "q_qkv"), pick("w_o", "q_o"), pick("w1", "q1"),
+                                           pick("w2", "q2"), dv["s_qkv"], dv["s_o"], dv["s1"], dv["s2"],
+                                           codes_int8=ab))
+            nbytes = H.h3dit_workspace_size(shape, n, tr)
+            ws = torch.empty(nbytes, device="cuda", dtype=torch.uint8)
+            xb = dev_bf16(x)
+            H.h3dit_block_forward(shape, bws[0], mods[0], xb, pos, n, ws, nbytes)
+            xs = dev_bf16(x)
+            H.h3dit_step_forward(shape, bws, mods, xs, pos, n, tr, ws, nbytes)
+            H.h3dit_check_device_error()
+            outs[as_bytes] = (xb, xs)
+        assert torch.equal(outs[False][0], outs[True][0])
+        assert torch.equal(outs[False][1], outs[True][1])
+        assert rel_l2(host(outs[True][0]), x) > 1e-3
