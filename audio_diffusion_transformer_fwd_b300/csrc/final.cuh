@@ -44,13 +44,27 @@ __host__ __device__ constexpr uint32_t head_stage_bytes(int c_out) {
 __host__ __device__ constexpr uint32_t head_mod_offset(int c_out) {
   return static_cast<uint32_t>(kHeadXBytes + c_out * kHeadBK * 2);
 }
-__host__ __device__ constexpr int head_stages(int c_out) {
-  return static_cast<int>(kHeadSmemLimit / head_stage_bytes(c_out)) < kHeadMaxStages
-             ? static_cast<int>(kHeadSmemLimit / head_stage_bytes(c_out))
-             : kHeadMaxStages;
+// The epilogue parks a CTA's fp32 partial sums (128 rows of c_out + 4
+// floats) over the stage buffers, so the ring is never smaller than that.
+__host__ __device__ constexpr uint32_t head_part_bytes(int c_out) {
+  return static_cast<uint32_t>(128 * (c_out + 4) * 4);
 }
+__host__ __device__ constexpr int head_stages(int c_out) {
+  const int fit = static_cast<int>(kHeadSmemLimit / head_stage_bytes(c_out)) < kHeadMaxStages
+                      ? static_cast<int>(kHeadSmemLimit / head_stage_bytes(c_out))
+                      : kHeadMaxStages;
+  const int need = static_cast<int>((head_part_bytes(c_out) + head_stage_bytes(c_out) - 1) / head_stage_bytes(c_out));
+  return fit > need ? fit : need;
+}
+static_assert(head_stages(kHeadMaxN) <= kHeadMaxStages, "the widest head's partial sums fit the ring");
 __host__ __device__ constexpr size_t head_smem_bytes(int c_out) {
   return 1024 + static_cast<size_t>(head_stages(c_out)) * head_stage_bytes(c_out) + 512;
+}
+// the most any supported width (16 .. kHeadMaxN, multiples of 16) asks for
+constexpr size_t head_smem_max() {
+  size_t m = 0;
+  for (int c = 16; c <= kHeadMaxN; c += 16) m = head_smem_bytes(c) > m ? head_smem_bytes(c) : m;
+  return m;
 }
 
 constexpr int kMaxHeads = 4;

@@ -1305,7 +1305,7 @@ h3dit_status h3dit_final_layer(const h3dit_config* cfg, const void* x, int n_tok
     if (!aligned(h.w, 16) || !aligned(h.out, 16) || !aligned(h.shift, 16) || !aligned(h.scale, 16))
       return fail(H3DIT_E_INVAL, "head %d tensors must be 16-byte aligned", i);
   }
-  H3_TRY(set_smem(h3::final_head_kernel, h3::kHeadSmemLimit + 1536));
+  H3_TRY(set_smem(h3::final_head_kernel, h3::head_smem_max()));
   h3::HeadBatch hb{};
   {
     const uint64_t dims[2] = {(uint64_t)d, (uint64_t)n_tokens};
@@ -1335,6 +1335,8 @@ h3dit_status h3dit_final_layer(const h3dit_config* cfg, const void* x, int n_tok
     while (cols < (uint32_t)h.c_out) cols <<= 1;
     a.tmem_cols = cols;
     a.stages = h3::head_stages(h.c_out);
+    if ((size_t)a.stages * h3::head_stage_bytes(h.c_out) < h3::head_part_bytes(h.c_out))
+      return fail(H3DIT_E_UNSUPPORTED, "head %d: c_out %d partial sums exceed the stage ring", i, h.c_out);
     max_tiles = std::max(max_tiles, (h.rows + 127) / 128);
     all_tiles += (h.rows + 127) / 128;
     smem = std::max(smem, h3::head_smem_bytes(h.c_out));
