@@ -57,6 +57,11 @@ struct GemmArgs {
   // thread's wait on that stage runs out (see h3dit_test_stall_next_gemm).
   int stall_kb;
   int band_n;   // tile raster: output tiles are walked in bands of band_n N-tiles, M fastest within a band
+  // CTA-pair kernel: tiles full_tiles .. num_tiles-1 (a last wave that would
+  // leave at least half of the pairs idle) are computed as two 256 x 128
+  // halves each; num_units = full_tiles + 2 * (num_tiles - full_tiles).
+  // Other kernels walk num_tiles whole tiles.
+  int full_tiles, num_units;
 };
 
 __device__ __forceinline__ float gelu_tanh_f(float x) {
@@ -276,6 +281,9 @@ namespace h3 {
 // full barrier, which both CTAs' copies complete; the MMA commit arrives on
 // the empty (and accumulator-full) barriers of both CTAs; the epilogue
 // threads of both CTAs arrive on rank 0's accumulator-empty barrier.
+// Tail: when the last wave of whole tiles would occupy at most half of the
+// pairs, those tiles are split into 256 x 128 halves (M256 N128 MMAs, each
+// CTA loading 64 weight rows), so twice as many pairs share the last wave.
 constexpr int kPairStages = 6;
 constexpr int kPairRows = 128;                       // A rows and B rows per CTA per tile
 constexpr int kPairABytes = kPairRows * kGemmBK * 2;  // 16 KB
@@ -283,10 +291,24 @@ constexpr int kPairBBytes = kPairRows * kGemmBK * 2;  // 16 KB
 constexpr int kPairStageBytes = kPairABytes + kPairBBytes;
 constexpr size_t kPairSmemBytes = 1024 + kPairStages * kPairStageBytes + 256;
 
+// Work unit u of the CTA-pair kernel: a whole 256 x 256 tile (half = -1) or
+// the left (0) / right (1) 128 columns of one.  Every output element is the
+// same k-ordered sum either way.
+__device__ __forceinline__ void pair_unit(int u, const GemmArgs& a, int& mb, int& nb, int& half) {
+  if (u < a.full_tiles) {
+    gemm_tile_coords(u, a, mb, nb);
+    half = -1;
+  } else {
+    const int h = u - a.full_tiles;
+    gemm_tile_coords(a.full_tiles + (h >> 1), a, mb, nb);
+    half = h & 1;
+  }
+}
+
 template <int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                          const GemmArgs args) {
+                          const __grid_constant__ CUtensorMap tmBh, const GemmArgs args) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -344,18 +366,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       const int stall_kb = blockIdx.x == 0 ? args.stall_kb : -1;
-      for (int t = cluster; t < args.num_tiles && ok; t += clusters) {
-        int mb, nb;
-        gemm_tile_coords(t, args, mb, nb);
+      for (int u = cluster; u < args.num_units && ok; u += clusters) {
+        int mb, nb, half;
+        pair_unit(u, args, mb, nb, half);
+        // a half unit: 64 of its 128 weight rows per CTA
+        const uint32_t bytes = half < 0 ? 2 * kPairStageBytes : 2 * (kPairABytes + kPairBBytes / 2);
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (t == cluster && kb == stall_kb) { ok = false; break; }
+          if (u == cluster && kb == stall_kb) { ok = false; break; }
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
-          if (rank == 0) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * kPairStageBytes);
+          if (rank == 0) mbar_arrive_expect_tx(full0 + 8 * stage, bytes);
           const uint32_t fb = full0_lead + 8 * stage;
           tma_load_2d_pair(smem_u32(sA + stage * kPairABytes), &tmA, fb, kb * kGemmBK,
                            mb * (2 * kPairRows) + rank * kPairRows);
-          tma_load_2d_pair(smem_u32(sB + stage * kPairBBytes), &tmB, fb, kb * kGemmBK,
-                           nb * kGemmBN + rank * kPairRows);
+          if (half < 0)
+            tma_load_2d_pair(smem_u32(sB + stage * kPairBBytes), &tmB, fb, kb * kGemmBK,
+                             nb * kGemmBN + rank * kPairRows);
+          else
+            tma_load_2d_pair(smem_u32(sB + stage * kPairBBytes), &tmBh, fb, kb * kGemmBK,
+                             nb * kGemmBN + half * (kGemmBN / 2) + rank * (kPairRows / 2));
           if (++stage == kPairStages) { stage = 0; phase ^= 1; }
         }
       }
@@ -368,14 +396,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ---------------- MMA issuer (rank 0 of the pair)
-      constexpr uint32_t idesc = idesc_bf16_f32(2 * kPairRows, kGemmBN);
+      constexpr uint32_t idesc_full = idesc_bf16_f32(2 * kPairRows, kGemmBN);
+      constexpr uint32_t idesc_half = idesc_bf16_f32(2 * kPairRows, kGemmBN / 2);
       const uint32_t a_lo0 = sdesc_lo(smem_u32(sA));
       const uint32_t b_lo0 = sdesc_lo(smem_u32(sB));
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
-      for (int t = cluster; t < args.num_tiles && ok; t += clusters, ++it) {
+      for (int u = cluster; u < args.num_units && ok; u += clusters, ++it) {
+        const uint32_t idesc = u < args.full_tiles ? idesc_full : idesc_half;
         const int acc = it & 1;
         if (!mbar_wait(tempty0 + 8 * acc, ((it >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
@@ -403,19 +433,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     int it = 0;
-    for (int t = cluster; t < args.num_tiles; t += clusters, ++it) {
-      int mb, nb;
-      gemm_tile_coords(t, args, mb, nb);
+    for (int u = cluster; u < args.num_units; u += clusters, ++it) {
+      int mb, nb, half;
+      pair_unit(u, args, mb, nb, half);
       const int acc = it & 1;
       if (!mbar_wait(tfull0 + 8 * acc, (it >> 1) & 1, abort_flag)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kGemmBN;
       const int grow = mb * (2 * kPairRows) + static_cast<int>(rank) * kPairRows + row;
+      const int col0 = nb * kGemmBN + (half < 0 ? 0 : half * (kGemmBN / 2));
+      const int chunks = (half < 0 ? kGemmBN : kGemmBN / 2) / 32;
 #pragma unroll 1
-      for (int c = 0; c < kGemmBN / 32; ++c) {
+      for (int c = 0; c < chunks; ++c) {
         float v[32];
         tmem_ld32(tbase + c * 32, v);
-        gemm_epilogue_chunk<EPI>(args, v, grow, nb * kGemmBN + c * 32);
+        gemm_epilogue_chunk<EPI>(args, v, grow, col0 + c * 32);
       }
       tc_fence_before();
       mbar_arrive_cluster(tempty0_lead + 8 * acc);

@@ -311,6 +311,8 @@ h3dit_status gemm_setup(const void* A, const void* B, int M, int N, int K, CUten
   args.tiles_m = (M + h3::kGemmBM - 1) / h3::kGemmBM;
   args.tiles_n = N / h3::kGemmBN;
   args.num_tiles = args.tiles_m * args.tiles_n;
+  args.full_tiles = args.num_tiles;
+  args.num_units = args.num_tiles;
   return H3DIT_OK;
 }
 
@@ -381,11 +383,25 @@ h3dit_status launch_on_pairs(K kernel, int threads, size_t smem_bytes, int tiles
   return H3DIT_OK;
 }
 
+// The last wave of whole tiles split into 256 x 128 halves when it would
+// leave at least half of the pairs idle (default; H3DIT_GEMM_TAIL=0 keeps
+// whole tiles, an A/B switch read at every launch).
+bool gemm_tail_split() {
+  const char* e = getenv("H3DIT_GEMM_TAIL");
+  return !(e && e[0] == '0');
+}
+
 template <int EPI>
-h3dit_status launch_pair_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const h3::GemmArgs& args,
-                                cudaStream_t s) {
-  return launch_on_pairs(h3::gemm_bf16_pair_kernel<EPI>, h3::kGemmThreads, h3::kPairSmemBytes, args.num_tiles, s,
-                         ta, tb, args);
+h3dit_status launch_pair_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbh,
+                                h3::GemmArgs args, cudaStream_t s) {
+  auto kernel = h3::gemm_bf16_pair_kernel<EPI>;
+  H3_TRY(set_smem(kernel, h3::kPairSmemBytes));
+  int fit = 0;
+  H3_TRY(pair_clusters(kernel, h3::kGemmThreads, h3::kPairSmemBytes, &fit));
+  const int rem = args.num_tiles % fit;
+  if (gemm_tail_split() && args.num_tiles > fit && rem > 0 && 2 * rem <= fit) args.full_tiles = args.num_tiles - rem;
+  args.num_units = args.full_tiles + 2 * (args.num_tiles - args.full_tiles);
+  return launch_on_pairs(kernel, h3::kGemmThreads, h3::kPairSmemBytes, args.num_units, s, ta, tb, tbh, args);
 }
 
 // Tensor maps and tile counts of a projection on CTA pairs: 256 x 256
@@ -416,20 +432,29 @@ h3dit_status pair_setup(const void* A, const void* B, int M, int N, int K, CUten
   args.tiles_m = (M + 2 * h3::kPairRows - 1) / (2 * h3::kPairRows);
   args.tiles_n = N / h3::kGemmBN;
   args.num_tiles = args.tiles_m * args.tiles_n;
+  args.full_tiles = args.num_tiles;
+  args.num_units = args.num_tiles;
   return H3DIT_OK;
 }
 
 h3dit_status launch_gemm_pair(int epi, const void* A, const void* B, int M, int N, int K, h3::GemmArgs args,
                               int cls, cudaStream_t s) {
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tbh;
   H3_TRY(pair_setup(A, B, M, N, K, ta, tb, args));
+  {
+    // weight tiles of a half unit: 64 rows per CTA
+    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)N};
+    const uint64_t str[1] = {(uint64_t)K * 2};
+    const uint32_t box[2] = {h3::kGemmBK, h3::kPairRows / 2};
+    H3_TRY(make_map(&tbh, B, 2, dims, str, box));
+  }
   args.stall_kb = take_stall_request();
   if (args.stall_kb >= K / h3::kGemmBK) args.stall_kb = -1;
   TimedLaunch tl(cls, s);
   switch (epi) {
-    case h3::kEpiStore: H3_TRY(launch_pair_kernel<h3::kEpiStore>(ta, tb, args, s)); break;
-    case h3::kEpiGelu: H3_TRY(launch_pair_kernel<h3::kEpiGelu>(ta, tb, args, s)); break;
-    case h3::kEpiQKV: H3_TRY(launch_pair_kernel<h3::kEpiQKV>(ta, tb, args, s)); break;
+    case h3::kEpiStore: H3_TRY(launch_pair_kernel<h3::kEpiStore>(ta, tb, tbh, args, s)); break;
+    case h3::kEpiGelu: H3_TRY(launch_pair_kernel<h3::kEpiGelu>(ta, tb, tbh, args, s)); break;
+    case h3::kEpiQKV: H3_TRY(launch_pair_kernel<h3::kEpiQKV>(ta, tb, tbh, args, s)); break;
     default: return fail(H3DIT_E_INVAL, "unknown epilogue %d", epi);
   }
   H3_CUDA(cudaGetLastError());

@@ -279,3 +279,57 @@ def test_pair_and_single_cta_projection_agree_bit_for_bit(monkeypatch, m, n, k, 
     if act:
         ref = O.bf16_round(O.gelu_tanh(host(a) @ host(b).T))
     assert rel_l2(host(out[1]), ref) <= 5e-3
+
+
+@pytest.mark.parametrize("act", [0, 1])
+def test_projection_tail_halves_equal_whole_tiles(monkeypatch, act):
+    """81 tiles of 256 x 256 (27 x 3, ragged M) on the device's CTA pairs
+    leave a short last wave, which the pair kernel runs as 256 x 128 halves
+    (twice as many pairs busy).  Each output is the same k-ordered sum as in
+    a whole tile, so the result equals whole tiles everywhere
+    (H3DIT_GEMM_TAIL=0) bit for bit, every element written, and both follow
+    the oracle; the single-CTA kernel agrees too."""
+    m, n, k = 6900, 768, 320
+    r = np.random.default_rng(61 + act)
+    a = synth.to_bf16_values(r.standard_normal((m, k)).astype(np.float32))
+    b = synth.to_bf16_values(r.standard_normal((n, k)).astype(np.float32) * 0.05)
+    ad, bd = dev_bf16(a), dev_bf16(b)
+    outs = []
+    for tail, single in (("1", "0"), ("0", "0"), ("1", "1")):
+        monkeypatch.setenv("H3DIT_GEMM_TAIL", tail)
+        monkeypatch.setenv("H3DIT_GEMM_SINGLE_CTA", single)
+        c = torch.full((m, n), float("nan"), device="cuda", dtype=torch.bfloat16)
+        H.h3dit_linear(ad, bd, m, n, k, act, c)
+        H.h3dit_check_device_error()
+        outs.append(c)
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    ref = a.astype(np.float64) @ b.astype(np.float64).T
+    if act:
+        ref = O.gelu_tanh(ref)
+    _close(host(outs[0]), ref)
+
+
+def test_qkv_projection_tail_halves_equal_whole_tiles(monkeypatch):
+    """The QKV epilogue (RoPE, head-major Q/K, transposed V) on half tiles:
+    6912 tokens, d 512 (162 tiles, a short last wave) give the same Q, K and
+    V^T with and without the split."""
+    n, d, heads, dh = 6912, 512, 4, 128
+    shape = H.BlockShape(d, heads, dh, 4 * d)
+    r = np.random.default_rng(63)
+    h = dev_bf16(r.standard_normal((n, d)).astype(np.float32))
+    w = dev_bf16(r.standard_normal((3 * d, d)).astype(np.float32) * 0.05)
+    pos = dev_f32(synth.positions((6, 32, 32), 512, 256))
+    table = torch.empty((n, dh // 2, 2), device="cuda", dtype=torch.float32)
+    H.h3dit_rope_table(shape, pos, n, table)
+    outs = []
+    for tail in ("1", "0"):
+        monkeypatch.setenv("H3DIT_GEMM_TAIL", tail)
+        q = torch.full((heads, n, dh), float("nan"), device="cuda", dtype=torch.bfloat16)
+        k = torch.full_like(q, float("nan"))
+        vt = torch.full((heads, dh, n), float("nan"), device="cuda", dtype=torch.bfloat16)
+        H.h3dit_qkv_project(shape, h, w, table, n, q, k, vt, n)
+        H.h3dit_check_device_error()
+        outs.append((q, k, vt))
+    for x, y in zip(*outs):
+        assert torch.equal(x, y)
+        assert not torch.isnan(x.float()).any()
