@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   // TMEM columns: S_0 (and P_0) at 0, S_1 (and P_1) at 128, O_0 at 256, O_1 at 256 + DH
+  grid_dep_wait();
 
   if (warp == 0) {
     if (lane == 0) {

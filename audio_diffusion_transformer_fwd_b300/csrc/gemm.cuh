@@ -180,6 +180,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const int kblocks = args.K / kGemmBK;
+  grid_dep_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -362,6 +363,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const int kblocks = args.K / kGemmBK;
+  grid_dep_wait();
   const uint32_t full0_lead = mapa_shared(full0, 0);
   const uint32_t tempty0_lead = mapa_shared(tempty0, 0);
 

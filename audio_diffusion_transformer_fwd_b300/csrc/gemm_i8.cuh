@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(kI8Threads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const int kblocks = args.K / kGemmBK;
+  grid_dep_wait();
   const int nchunks = (kblocks + qa.chunk_kb - 1) / qa.chunk_kb;
   const uint32_t full0_lead = PAIR ? mapa_shared(full0, 0) : full0;
   const uint32_t tempty0_lead = PAIR ? mapa_shared(tempty0, 0) : tempty0;

@@ -123,6 +123,19 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ----------------------------------------------------------------- launch overlap
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may be scheduled as the kernel before it on the stream
+// retires its CTAs; it must call grid_dep_wait() before its first access to
+// global memory, which returns once that kernel has completed and its
+// writes are visible (so no earlier kernel still reads what it writes).
+// Only shared-memory barrier setup, tensor-memory allocation and tensor-map
+// prefetches (kernel parameters) come before it.  No kernel signals its
+// dependents early (measured slower: the early CTAs crowd the running
+// grid), so they are scheduled as its CTAs exit.  In a kernel launched
+// without the attribute the wait is a no-op.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ----------------------------------------------------------------- clusters
 // Every thread of every CTA of the cluster; orders shared-memory writes
 // before the barrier with reads (local or distributed) after it.

@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(kRowThreads, row_min_blocks<GATE, NORM, QUANT,
                       const float* __restrict__ gate, const float* __restrict__ shift,
                       const float* __restrict__ scale, __nv_bfloat16* __restrict__ h,
                       float* __restrict__ hs, int d, float eps, SegMap sm) {
+  grid_dep_wait();
   __shared__ float red[4];
   const size_t row = blockIdx.x;
   if (sm.count > 1) {
@@ -266,6 +267,7 @@ __global__ void __launch_bounds__(kRowThreads, row_min_blocks<GATE, NORM, QUANT,
 __global__ void __launch_bounds__(kRowThreads)
     quantize_codes_kernel(const __nv_bfloat16* x, int cols, int group, __nv_bfloat16* q,
                           float* __restrict__ scales) {
+  grid_dep_wait();
   __shared__ float red[4];
   const int groups = cols / group;
   const size_t row = blockIdx.x / groups;
@@ -301,6 +303,7 @@ template <int NV, bool CODES>
 __global__ void __launch_bounds__(256)
     quantize_warp_kernel(const __nv_bfloat16* x, int cols, int group, long long n_groups, __nv_bfloat16* q16,
                          int8_t* q8, float* __restrict__ scales) {
+  grid_dep_wait();
   const long long gw = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   if (gw >= n_groups) return;
   const int lane = threadIdx.x & 31;
@@ -341,6 +344,7 @@ __global__ void __launch_bounds__(256)
 // int8 codes -> the same integers as BF16 values (exact), 8 per thread.
 __global__ void widen_codes_kernel(const int8_t* __restrict__ q, size_t n8,
                                    __nv_bfloat16* __restrict__ out) {
+  grid_dep_wait();
   const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n8) return;
   const uint2 w = reinterpret_cast<const uint2*>(q)[i];
@@ -535,6 +539,7 @@ struct RopeSpec {
 
 __global__ void rope_table_kernel(const float* __restrict__ pos, int n, RopeSpec rs,
                                   float2* __restrict__ table) {
+  grid_dep_wait();
   const int half = rs.head_dim / 2;
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= n * half) return;

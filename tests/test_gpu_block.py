@@ -245,3 +245,49 @@ def test_step_replays_from_a_cuda_graph():
         torch.cuda.synchronize()
         H.h3dit_check_device_error()
         assert torch.equal(xg, eager)
+
+
+@pytest.mark.parametrize("precision", ["bf16", "int8"])
+def test_overlapped_launches_equal_stream_order(monkeypatch, precision):
+    """The step's kernels are launched with programmatic stream
+    serialisation (each may start its prologue while the previous kernel
+    retires, then waits for it before touching global memory).  A reduced
+    5-block step, and a step that follows a torch kernel writing its input,
+    give the same bits as plain stream order (H3DIT_PDL=0)."""
+    w = TINY
+    n = w.n_tokens
+    prec = H.INT8 if precision == "int8" else H.BF16
+    shape = shape_of(w, prec)
+    pos = dev_f32(synth.positions(w.video, w.n_text, w.n_audio))
+    nb = 5
+    keep, bws = [], []
+    for b in range(nb):
+        wt = synth.host_block_weights(w.d, w.ffn, seed=71, block=b)
+        if prec == H.INT8:
+            dv = {}
+            for name in ("w_qkv", "w_o", "w1", "w2"):
+                q, s = O.quantize_weight(wt[name])
+                dv[name], dv[name + "_s"] = dev_bf16(q.astype(np.float32)), dev_f32(s[:, 0])
+            bws.append(H.block_weights(dv["w_qkv"], dv["w_o"], dv["w1"], dv["w2"],
+                                       dv["w_qkv_s"], dv["w_o_s"], dv["w1_s"], dv["w2_s"]))
+        else:
+            dv, bw = _weights_dev(wt)
+            bws.append(bw)
+        keep.append(dv)
+    mods = dev_f32(np.stack([synth.host_mod(w.d, seed=71, block=b) for b in range(nb)]))
+    x = synth.host_activations(n, w.d, seed=71)
+    T, Hh, W = w.video
+    tr = H.reduction(H.video_grid(0, T, Hh, W), 1, 3)
+    nbytes = H.h3dit_workspace_size(shape, n, tr)
+    ws = torch.empty(nbytes, device="cuda", dtype=torch.uint8)
+    outs = []
+    for pdl in ("1", "0"):
+        monkeypatch.setenv("H3DIT_PDL", pdl)
+        xs = torch.zeros((n, w.d), device="cuda", dtype=torch.bfloat16)
+        xs.copy_(dev_bf16(x))            # a torch kernel writes the step's input just before it
+        ws.fill_(0xFF)
+        H.h3dit_step_forward(shape, bws, mods, xs, pos, n, tr, ws, nbytes)
+        H.h3dit_check_device_error()
+        outs.append(xs)
+    assert torch.equal(outs[0], outs[1])
+    assert rel_l2(host(outs[0]), x) > 1e-3
