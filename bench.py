@@ -375,6 +375,16 @@ def run_ours(args):
         "row_kernels": {"ms": rows_ms, "note": "rope table + AdaLN-1 + gated residual fused with AdaLN-2 + "
                         "final gated residual per block"},
     }
+    # attention's second roofline: one exponential per score (N^2 per head)
+    # on the MUFU pipe, 16 results per clock per SM, at the run's median SM clock
+    sm_mhz = clocks.get("sm_mhz") if isinstance(clocks, dict) else None
+    if sm_mhz and attn_ms > 0:
+        n_sm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+        exps = float(n) * n * w.heads
+        kernels["attention"]["mufu"] = {
+            "exp2_per_block": exps, "rate": f"16 per clock per SM x {n_sm} SMs at {sm_mhz:.0f} MHz",
+            "min_ms": exps / (16.0 * n_sm * sm_mhz * 1e6) * 1e3,
+            "frac": exps / (attn_ms * 1e-3) / (16.0 * n_sm * sm_mhz * 1e6)}
     # algorithmic bytes of the row kernels of one block: AdaLN-1 reads x and
     # writes h (4 N d), the fused gated residual + AdaLN-2 reads x and the
     # branch and writes x and h2 (8 N d), the final gated residual reads x and
