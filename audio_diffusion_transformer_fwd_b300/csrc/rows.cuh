@@ -11,11 +11,13 @@ namespace h3 {
 constexpr int kRowThreads = 128;
 constexpr int kRowMaxVec = 8;   // 8 x 128 threads x 8 values = 8192 columns
 
+// Sum over the 128 threads of the CTA.  red[4] must be this reduction's
+// own shared slots (not read by an earlier reduction of the same row), so a
+// single barrier suffices.
 __device__ __forceinline__ float block_sum_128(float v, float* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   const int w = threadIdx.x >> 5;
-  __syncthreads();   // red[] may still be read by a previous reduction
   if ((threadIdx.x & 31) == 0) red[w] = v;
   __syncthreads();
   return red[0] + red[1] + red[2] + red[3];
@@ -145,7 +147,7 @@ __global__ void __launch_bounds__(kRowThreads, row_min_blocks<GATE, NORM, QUANT,
                       const float* __restrict__ scale, __nv_bfloat16* __restrict__ h,
                       float* __restrict__ hs, int d, float eps, SegMap sm) {
   grid_dep_wait();
-  __shared__ float red[4];
+  __shared__ float red[12];   // mean, variance and absmax: four slots each
   const size_t row = blockIdx.x;
   if (sm.count > 1) {
     const int so = seg_offset(sm, static_cast<int>(row));
@@ -202,7 +204,7 @@ __global__ void __launch_bounds__(kRowThreads, row_min_blocks<GATE, NORM, QUANT,
       }
     }
   }
-  const float var = block_sum_128(sq, red) / static_cast<float>(d);
+  const float var = block_sum_128(sq, red + 4) / static_cast<float>(d);
   const float rstd = rsqrtf(var + eps);
   uint4* hr = reinterpret_cast<uint4*>(h + row * d);
 #pragma unroll
@@ -241,10 +243,9 @@ __global__ void __launch_bounds__(kRowThreads, row_min_blocks<GATE, NORM, QUANT,
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  __syncthreads();   // red[] was last read by the variance reduction
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  if ((threadIdx.x & 31) == 0) red[8 + (threadIdx.x >> 5)] = amax;
   __syncthreads();
-  amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  amax = fmaxf(fmaxf(red[8], red[9]), fmaxf(red[10], red[11]));
   const QuantScale sq8 = quant_scale(__fdiv_rn(amax, 127.0f));
   if (threadIdx.x == 0) hs[row] = sq8.s;
 #pragma unroll
