@@ -90,12 +90,13 @@ __device__ __forceinline__ void i8_epilogue16(const GemmArgs& a, const float (&v
 // projections run (gemm.cuh): 256 x 256 tiles over two SMs, each CTA
 // streaming its 128 A rows and 128 of the 256 weight rows per k-block into
 // a 6-deep ring, rank 0 issuing M = 256 MMAs, each CTA's eight epilogue
-// warps draining its own 128 rows of every chunk.
+// warps draining its own 128 rows of every chunk.  A short last wave runs
+// as 256 x 128 half tiles (pair_unit), drained by the column-half-0 warps.
 template <int EPI, int MODE, bool PAIR>
 __global__ void __launch_bounds__(kI8Threads, 1)
     gemm_i8x_tc_kernel(const __grid_constant__ CUtensorMap tmA,
-                       const __grid_constant__ CUtensorMap tmB, const GemmArgs args,
-                       const I8Args qa) {
+                       const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBh,
+                       const GemmArgs args, const I8Args qa) {
   constexpr int kStages = PAIR ? kPairStages : kGemmStages;
   constexpr int kABytes = PAIR ? kPairABytes : kGemmABytes;
   constexpr int kBBytes = PAIR ? kPairBBytes : kGemmBBytes;
@@ -155,6 +156,9 @@ __global__ void __launch_bounds__(kI8Threads, 1)
   grid_dep_wait();
   const int nchunks = (kblocks + qa.chunk_kb - 1) / qa.chunk_kb;
   const uint32_t full0_lead = PAIR ? mapa_shared(full0, 0) : full0;
+  // work units: whole tiles, and on CTA pairs the 256 x 128 halves of a
+  // short last wave (pair_unit; the single-CTA launch has whole tiles only)
+  const int units = PAIR ? args.num_units : args.num_tiles;
   const uint32_t tempty0_lead = PAIR ? mapa_shared(tempty0, 0) : tempty0;
 
   if (warp == 0) {
@@ -163,18 +167,23 @@ __global__ void __launch_bounds__(kI8Threads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int t = first; t < args.num_tiles && ok; t += step) {
-        int mb, nb;
-        gemm_tile_coords(t, args, mb, nb);
+      for (int u = first; u < units && ok; u += step) {
+        int mb, nb, half;
+        pair_unit(u, args, mb, nb, half);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
           if constexpr (PAIR) {
-            if (rank == 0) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * (kABytes + kBBytes));
+            if (rank == 0)
+              mbar_arrive_expect_tx(full0 + 8 * stage, half < 0 ? 2 * (kABytes + kBBytes) : 2 * (kABytes + kBBytes / 2));
             const uint32_t fb = full0_lead + 8 * stage;
             tma_load_2d_pair(smem_u32(sA + stage * kABytes), &tmA, fb, kb * kGemmBK,
                              mb * kTileM + static_cast<int>(rank) * kPairRows);
-            tma_load_2d_pair(smem_u32(sB + stage * kBBytes), &tmB, fb, kb * kGemmBK,
-                             nb * kGemmBN + static_cast<int>(rank) * kPairRows);
+            if (half < 0)
+              tma_load_2d_pair(smem_u32(sB + stage * kBBytes), &tmB, fb, kb * kGemmBK,
+                               nb * kGemmBN + static_cast<int>(rank) * kPairRows);
+            else
+              tma_load_2d_pair(smem_u32(sB + stage * kBBytes), &tmBh, fb, kb * kGemmBK,
+                               nb * kGemmBN + half * (kGemmBN / 2) + static_cast<int>(rank) * (kPairRows / 2));
           } else {
             const uint32_t fb = full0 + 8 * stage;
             mbar_arrive_expect_tx(fb, kABytes + kBBytes);
@@ -191,14 +200,16 @@ __global__ void __launch_bounds__(kI8Threads, 1)
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ---------------- MMA issuer: one accumulator per chunk, alternating
-      constexpr uint32_t idesc = idesc_bf16_f32(kTileM, kGemmBN);
+      constexpr uint32_t idesc_full = idesc_bf16_f32(kTileM, kGemmBN);
+      constexpr uint32_t idesc_half = idesc_bf16_f32(kTileM, kGemmBN / 2);
       const uint32_t a_lo0 = sdesc_lo(smem_u32(sA));
       const uint32_t b_lo0 = sdesc_lo(smem_u32(sB));
       int stage = 0;
       uint32_t phase = 0;
       int cc = 0;   // chunks issued so far by this CTA
       bool ok = true;
-      for (int t = first; t < args.num_tiles && ok; t += step) {
+      for (int u = first; u < units && ok; u += step) {
+        const uint32_t idesc = u < args.full_tiles ? idesc_full : idesc_half;
         for (int ch = 0; ch < nchunks && ok; ++ch, ++cc) {
           const int acc = cc & 1;
           if (!mbar_wait(tempty0 + 8 * acc, ((cc >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
@@ -237,12 +248,15 @@ __global__ void __launch_bounds__(kI8Threads, 1)
     const int row = quarter * 32 + lane;
     int cc = 0;
     bool ok = true;
-    for (int t = first; t < args.num_tiles && ok; t += step) {
-      int mb, nb;
-      gemm_tile_coords(t, args, mb, nb);
+    for (int u = first; u < units && ok; u += step) {
+      int mb, nb, unit_half;
+      pair_unit(u, args, mb, nb, unit_half);
       const int grow = mb * kTileM + static_cast<int>(rank) * kPairRows * (PAIR ? 1 : 0) + row;
-      const bool live = grow < args.M;
-      const int col0 = nb * kGemmBN + half * 128;
+      // a half unit's 128 columns are column half 0 of the accumulator: the
+      // other four warps only keep the barrier counts
+      const bool cols = unit_half < 0 || half == 0;
+      const bool live = cols && grow < args.M;
+      const int col0 = nb * kGemmBN + (unit_half < 0 ? half : unit_half) * 128;
       int iacc[128];
       float facc[128];
       for (int ch = 0; ch < nchunks; ++ch, ++cc) {
@@ -259,17 +273,19 @@ __global__ void __launch_bounds__(kI8Threads, 1)
         // 16 columns per TMEM load keeps the 128 running sums plus the
         // loaded values within the 168 registers a thread of this 10-warp
         // CTA can have (three warps share one SM sub-partition's registers)
+        if (cols) {   // warp-uniform: the tensor-memory loads are warp-collective
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          float v[16];
-          tmem_ld16(tbase + c8 * 16, v);
+          for (int c8 = 0; c8 < 8; ++c8) {
+            float v[16];
+            tmem_ld16(tbase + c8 * 16, v);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            if constexpr (MODE == kI8Int) {
-              const int x = __float2int_rn(v[i]);   // an exact integer below 2^24
-              iacc[c8 * 16 + i] = ch == 0 ? x : iacc[c8 * 16 + i] + x;
-            } else {
-              facc[c8 * 16 + i] = ch == 0 ? v[i] * sg : fmaf(v[i], sg, facc[c8 * 16 + i]);
+            for (int i = 0; i < 16; ++i) {
+              if constexpr (MODE == kI8Int) {
+                const int x = __float2int_rn(v[i]);   // an exact integer below 2^24
+                iacc[c8 * 16 + i] = ch == 0 ? x : iacc[c8 * 16 + i] + x;
+              } else {
+                facc[c8 * 16 + i] = ch == 0 ? v[i] * sg : fmaf(v[i], sg, facc[c8 * 16 + i]);
+              }
             }
           }
         }

@@ -418,6 +418,15 @@ bool gemm_tail_split() {
   return !(e && e[0] == '0');
 }
 
+// On `fit` co-resident pairs: the last wave of whole tiles becomes half
+// tiles when it would keep at most half of the pairs busy.
+void split_tail(h3::GemmArgs& args, int fit) {
+  const int rem = args.num_tiles % fit;
+  args.full_tiles = args.num_tiles;
+  if (gemm_tail_split() && args.num_tiles > fit && rem > 0 && 2 * rem <= fit) args.full_tiles = args.num_tiles - rem;
+  args.num_units = args.full_tiles + 2 * (args.num_tiles - args.full_tiles);
+}
+
 template <int EPI>
 h3dit_status launch_pair_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbh,
                                 h3::GemmArgs args, cudaStream_t s) {
@@ -425,9 +434,7 @@ h3dit_status launch_pair_kernel(const CUtensorMap& ta, const CUtensorMap& tb, co
   H3_TRY(set_smem(kernel, h3::kPairSmemBytes));
   int fit = 0;
   H3_TRY(pair_clusters(kernel, h3::kGemmThreads, h3::kPairSmemBytes, &fit));
-  const int rem = args.num_tiles % fit;
-  if (gemm_tail_split() && args.num_tiles > fit && rem > 0 && 2 * rem <= fit) args.full_tiles = args.num_tiles - rem;
-  args.num_units = args.full_tiles + 2 * (args.num_tiles - args.full_tiles);
+  split_tail(args, fit);
   return launch_on_pairs(kernel, h3::kGemmThreads, h3::kPairSmemBytes, args.num_units, s, ta, tb, tbh, args);
 }
 
@@ -464,17 +471,19 @@ h3dit_status pair_setup(const void* A, const void* B, int M, int N, int K, CUten
   return H3DIT_OK;
 }
 
+// Weight tiles of a half unit on CTA pairs: 64 rows per CTA.
+h3dit_status half_weight_map(const void* B, int N, int K, CUtensorMap& tbh) {
+  const uint64_t dims[2] = {(uint64_t)K, (uint64_t)N};
+  const uint64_t str[1] = {(uint64_t)K * 2};
+  const uint32_t box[2] = {h3::kGemmBK, h3::kPairRows / 2};
+  return make_map(&tbh, B, 2, dims, str, box);
+}
+
 h3dit_status launch_gemm_pair(int epi, const void* A, const void* B, int M, int N, int K, h3::GemmArgs args,
                               int cls, cudaStream_t s) {
   CUtensorMap ta, tb, tbh;
   H3_TRY(pair_setup(A, B, M, N, K, ta, tb, args));
-  {
-    // weight tiles of a half unit: 64 rows per CTA
-    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)N};
-    const uint64_t str[1] = {(uint64_t)K * 2};
-    const uint32_t box[2] = {h3::kGemmBK, h3::kPairRows / 2};
-    H3_TRY(make_map(&tbh, B, 2, dims, str, box));
-  }
+  H3_TRY(half_weight_map(B, N, K, tbh));
   args.stall_kb = take_stall_request();
   if (args.stall_kb >= K / h3::kGemmBK) args.stall_kb = -1;
   TimedLaunch tl(cls, s);
@@ -521,15 +530,20 @@ h3dit_status launch_gemm(int epi, const void* A, const void* B, int M, int N, in
 }
 
 template <int EPI, int MODE>
-h3dit_status launch_i8_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const h3::GemmArgs& args,
-                              const h3::I8Args& qa, bool pair, cudaStream_t s) {
+h3dit_status launch_i8_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbh,
+                              h3::GemmArgs args, const h3::I8Args& qa, bool pair, cudaStream_t s) {
   if (pair) {
-    H3_TRY(launch_on_pairs(h3::gemm_i8x_tc_kernel<EPI, MODE, true>, h3::kI8Threads, h3::kPairSmemBytes,
-                           args.num_tiles, s, ta, tb, args, qa));
+    auto kernel = h3::gemm_i8x_tc_kernel<EPI, MODE, true>;
+    H3_TRY(set_smem(kernel, h3::kPairSmemBytes));
+    int fit = 0;
+    H3_TRY(pair_clusters(kernel, h3::kI8Threads, h3::kPairSmemBytes, &fit));
+    split_tail(args, fit);
+    H3_TRY(launch_on_pairs(kernel, h3::kI8Threads, h3::kPairSmemBytes, args.num_units, s, ta, tb, tbh, args, qa));
   } else {
     const int grid = std::min(args.num_tiles, sm_count());
     H3_TRY(set_smem(h3::gemm_i8x_tc_kernel<EPI, MODE, false>, h3::kGemmSmemBytes));
-    h3::gemm_i8x_tc_kernel<EPI, MODE, false><<<grid, h3::kI8Threads, h3::kGemmSmemBytes, s>>>(ta, tb, args, qa);
+    h3::gemm_i8x_tc_kernel<EPI, MODE, false><<<grid, h3::kI8Threads, h3::kGemmSmemBytes, s>>>(ta, tb, tb, args,
+                                                                                              qa);
   }
   H3_CUDA(cudaGetLastError());
   return H3DIT_OK;
@@ -541,10 +555,15 @@ h3dit_status launch_i8_kernel(const CUtensorMap& ta, const CUtensorMap& tb, cons
 // group <= 1024).  epi kEpiAcc writes the raw int32 accumulators.
 h3dit_status launch_gemm_i8(int epi, const void* A, const float* sa, int group, const void* B, const float* sb,
                             int M, int N, int K, h3::GemmArgs args, int32_t* acc, int cls, cudaStream_t s) {
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tbh;
   const bool pair = gemm_pair_enabled();
-  if (pair) H3_TRY(pair_setup(A, B, M, N, K, ta, tb, args));
-  else H3_TRY(gemm_setup(A, B, M, N, K, ta, tb, args));
+  if (pair) {
+    H3_TRY(pair_setup(A, B, M, N, K, ta, tb, args));
+    H3_TRY(half_weight_map(B, N, K, tbh));
+  } else {
+    H3_TRY(gemm_setup(A, B, M, N, K, ta, tb, args));
+    tbh = tb;
+  }
   if (K > (1 << 17)) return fail(H3DIT_E_UNSUPPORTED, "int8 k %d (the int32 accumulator bound needs k <= 131072)", K);
   h3::I8Args qa{};
   qa.sa = sa;
@@ -566,16 +585,16 @@ h3dit_status launch_gemm_i8(int epi, const void* A, const float* sa, int group, 
   TimedLaunch tl(cls, s);
   if (grouped) {
     switch (epi) {
-      case h3::kEpiStore: return launch_i8_kernel<h3::kEpiStore, h3::kI8Group>(ta, tb, args, qa, pair, s);
-      case h3::kEpiGelu: return launch_i8_kernel<h3::kEpiGelu, h3::kI8Group>(ta, tb, args, qa, pair, s);
+      case h3::kEpiStore: return launch_i8_kernel<h3::kEpiStore, h3::kI8Group>(ta, tb, tbh, args, qa, pair, s);
+      case h3::kEpiGelu: return launch_i8_kernel<h3::kEpiGelu, h3::kI8Group>(ta, tb, tbh, args, qa, pair, s);
       default: return fail(H3DIT_E_INVAL, "grouped int8 epilogue %d", epi);
     }
   }
   switch (epi) {
-    case h3::kEpiStore: return launch_i8_kernel<h3::kEpiStore, h3::kI8Int>(ta, tb, args, qa, pair, s);
-    case h3::kEpiGelu: return launch_i8_kernel<h3::kEpiGelu, h3::kI8Int>(ta, tb, args, qa, pair, s);
-    case h3::kEpiQKV: return launch_i8_kernel<h3::kEpiQKV, h3::kI8Int>(ta, tb, args, qa, pair, s);
-    case h3::kEpiAcc: return launch_i8_kernel<h3::kEpiAcc, h3::kI8Int>(ta, tb, args, qa, pair, s);
+    case h3::kEpiStore: return launch_i8_kernel<h3::kEpiStore, h3::kI8Int>(ta, tb, tbh, args, qa, pair, s);
+    case h3::kEpiGelu: return launch_i8_kernel<h3::kEpiGelu, h3::kI8Int>(ta, tb, tbh, args, qa, pair, s);
+    case h3::kEpiQKV: return launch_i8_kernel<h3::kEpiQKV, h3::kI8Int>(ta, tb, tbh, args, qa, pair, s);
+    case h3::kEpiAcc: return launch_i8_kernel<h3::kEpiAcc, h3::kI8Int>(ta, tb, tbh, args, qa, pair, s);
     default: return fail(H3DIT_E_INVAL, "int8 epilogue %d", epi);
   }
 }

@@ -498,3 +498,60 @@ def test_int8_weights_as_bytes_equal_operand_form():
         assert torch.equal(outs[False][0], outs[True][0])
         assert torch.equal(outs[False][1], outs[True][1])
         assert rel_l2(host(outs[True][0]), x) > 1e-3
+
+
+def test_int8_projection_tail_halves_equal_whole_tiles(monkeypatch):
+    """The int8 CTA-pair kernel also runs a short last wave (81 tiles of
+    256 x 256) as 256 x 128 halves.  Per-row scales with int32 chunks, the
+    raw int32 accumulators, 1024-channel groups and the QKV epilogue give
+    the same bits with the split and without it (H3DIT_GEMM_TAIL=0), every
+    element written; the int32 accumulators also equal the exact integer
+    products."""
+    m, n, k = 6900, 768, 2048
+    r = np.random.default_rng(81)
+    a8 = r.integers(-127, 128, (m, k)).astype(np.int8)
+    b8 = r.integers(-127, 128, (n, k)).astype(np.int8)
+    ad, bd = codes_dev(a8), codes_dev(b8)
+    sa = dev_f32((r.random(m) * 0.01).astype(np.float32))
+    sg = dev_f32((r.random((m, k // 1024)) * 0.01).astype(np.float32))
+    sb = dev_f32((r.random(n) * 0.01).astype(np.float32))
+    outs = {}
+    for tail in ("1", "0"):
+        monkeypatch.setenv("H3DIT_GEMM_TAIL", tail)
+        c1 = torch.full((m, n), float("nan"), device="cuda", dtype=torch.bfloat16)
+        H.h3dit_linear_i8(ad, sa, k, bd, sb, m, n, k, 1, c1)
+        c2 = torch.full((m, n), float("nan"), device="cuda", dtype=torch.bfloat16)
+        H.h3dit_linear_i8(ad, sg, 1024, bd, sb, m, n, k, 0, c2)
+        acc = torch.full((m, n), -1, device="cuda", dtype=torch.int32)
+        H.h3dit_linear_i8_acc(ad, bd, m, n, k, acc)
+        H.h3dit_check_device_error()
+        outs[tail] = (c1, c2, acc)
+    for x, y in zip(outs["1"], outs["0"]):
+        assert torch.equal(x, y)
+    rows = np.array([0, 1, 255, 256, 3333, 6655, 6656, 6899])
+    exact = a8[rows].astype(np.int64) @ b8.astype(np.int64).T
+    assert np.array_equal(outs["1"][2].cpu().numpy()[rows], exact)
+    assert not torch.isnan(outs["1"][0].float()).any() and not torch.isnan(outs["1"][1].float()).any()
+
+    # the QKV + RoPE epilogue on half tiles: 6912 tokens, d 512 (162 tiles)
+    nt, d, heads, dh = 6912, 512, 4, 128
+    shape = H.BlockShape(d, heads, dh, 4 * d, precision=H.INT8)
+    hq = codes_dev(r.integers(-127, 128, (nt, d)).astype(np.int8))
+    hs = dev_f32((r.random(nt) * 0.01).astype(np.float32))
+    wq = codes_dev(r.integers(-127, 128, (3 * d, d)).astype(np.int8))
+    ws = dev_f32((r.random(3 * d) * 0.01).astype(np.float32))
+    pos = dev_f32(synth.positions((6, 32, 32), 512, 256))
+    table = torch.empty((nt, dh // 2, 2), device="cuda", dtype=torch.float32)
+    H.h3dit_rope_table(shape, pos, nt, table)
+    res = []
+    for tail in ("1", "0"):
+        monkeypatch.setenv("H3DIT_GEMM_TAIL", tail)
+        q = torch.full((heads, nt, dh), float("nan"), device="cuda", dtype=torch.bfloat16)
+        kk = torch.full_like(q, float("nan"))
+        vt = torch.full((heads, dh, nt), float("nan"), device="cuda", dtype=torch.bfloat16)
+        H.h3dit_qkv_project_i8(shape, hq, hs, wq, ws, table, nt, q, kk, vt, nt)
+        H.h3dit_check_device_error()
+        res.append((q, kk, vt))
+    for x, y in zip(*res):
+        assert torch.equal(x, y)
+        assert not torch.isnan(x.float()).any()
