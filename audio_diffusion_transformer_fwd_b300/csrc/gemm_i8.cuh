@@ -42,6 +42,49 @@ struct I8Args {
 
 // The epilogues of gemm_epilogue_chunk on 16 columns (a 16-column group
 // never straddles a head: head_dim is 64 or 128).
+// Where a thread's 128 output columns (col0, a multiple of 128) fall in the
+// QKV projection: its region (Q, K or V) and the column within that region
+// (head_dim is a power of two, so heads and head dims follow by shifts).
+struct QkvPlace {
+  int region, cin0, hd_shift;
+};
+__device__ __forceinline__ QkvPlace qkv_place(const GemmArgs& a, int col0) {
+  QkvPlace p;
+  p.region = col0 / a.d;   // d is a multiple of 256: 128 columns never straddle regions
+  p.cin0 = col0 - p.region * a.d;
+  p.hd_shift = a.head_dim == 128 ? 7 : 6;
+  return p;
+}
+
+// The QKV epilogue on 16 columns cin .. cin+15 of a region (they never
+// straddle a head): RoPE and head-major stores for Q and K (QK), V
+// transposed otherwise.
+template <bool QK>
+__device__ __forceinline__ void i8_qkv16(const GemmArgs& a, const float (&v)[16], int grow, const QkvPlace& pl,
+                                         int cin) {
+  const int head = cin >> pl.hd_shift;
+  const int dh0 = cin & (a.head_dim - 1);
+  if constexpr (QK) {
+    const float4* cs = reinterpret_cast<const float4*>(a.rope + static_cast<size_t>(grow) * (a.head_dim / 2) + dh0 / 2);
+    uint32_t p[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 t = __ldg(cs + i);   // (cos, sin) of two consecutive pairs
+      const float a0 = v[4 * i], b0 = v[4 * i + 1], a1 = v[4 * i + 2], b1 = v[4 * i + 3];
+      p[2 * i] = pack_bf16x2(a0 * t.x - b0 * t.y, a0 * t.y + b0 * t.x);
+      p[2 * i + 1] = pack_bf16x2(a1 * t.z - b1 * t.w, a1 * t.w + b1 * t.z);
+    }
+    __nv_bfloat16* base = pl.region == 0 ? a.q : a.k;
+    uint4* dst = reinterpret_cast<uint4*>(base + (static_cast<size_t>(head) * a.M + grow) * a.head_dim + dh0);
+    dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
+    dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+  } else {
+    __nv_bfloat16* dst = a.vt + (static_cast<size_t>(head) * a.head_dim + dh0) * a.vt_ld + grow;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) dst[static_cast<size_t>(i) * a.vt_ld] = __float2bfloat16_rn(v[i]);
+  }
+}
+
 template <int EPI>
 __device__ __forceinline__ void i8_epilogue16(const GemmArgs& a, const float (&v)[16], int grow, int gcol) {
   if constexpr (EPI == kEpiStore || EPI == kEpiGelu) {
@@ -307,9 +350,8 @@ __global__ void __launch_bounds__(kI8Threads, 1)
       } else {
         float sa = 1.f;
         if constexpr (MODE == kI8Int) sa = __ldg(qa.sa + grow);
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          float v[16];
+        // the 16 dequantised values of column group c8
+        auto group16 = [&](int c8, float (&v)[16]) {
           const float4* sb4 = reinterpret_cast<const float4*>(qa.sb + col0 + c8 * 16);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -322,7 +364,37 @@ __global__ void __launch_bounds__(kI8Threads, 1)
               else v[4 * i + e] = facc[j] * sbv[e];
             }
           }
-          i8_epilogue16<EPI>(args, v, grow, col0 + c8 * 16);
+        };
+        if constexpr (EPI == kEpiQKV) {
+          // the region is the same for all 128 columns: one loop per region
+          // keeps the unrolled code (and its registers) to one epilogue form
+          const QkvPlace pl = qkv_place(args, col0);
+          if (pl.region < 2) {
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+              float v[16];
+              group16(c8, v);
+              i8_qkv16<true>(args, v, grow, pl, pl.cin0 + c8 * 16);
+              // keep the next group's loads behind this group's stores:
+              // hoisting them would need registers the running sums hold
+              asm volatile("" ::: "memory");
+            }
+          } else {
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+              float v[16];
+              group16(c8, v);
+              i8_qkv16<false>(args, v, grow, pl, pl.cin0 + c8 * 16);
+              asm volatile("" ::: "memory");
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8) {
+            float v[16];
+            group16(c8, v);
+            i8_epilogue16<EPI>(args, v, grow, col0 + c8 * 16);
+          }
         }
       }
     }
