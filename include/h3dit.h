@@ -165,6 +165,18 @@ int h3dit_version(void);
  * if set, H3DIT_E_CUDA if the synchronisation itself failed. */
 h3dit_status h3dit_check_device_error(cudaStream_t stream);
 
+/* Launch behaviour.  Calls are asynchronous and stream-ordered.  The block
+ * and step kernels are launched with programmatic stream serialisation:
+ * each may be scheduled while the kernel before it on the stream retires
+ * its CTAs, and waits for that kernel (griddepcontrol.wait) before it
+ * touches global memory, so the results are those of plain stream order.
+ * Environment switches for A/B measurement only (all give the same bits;
+ * read at every call, H3DIT_DISABLE_GATED_ADALN once per process): H3DIT_PDL=0 plain launches; H3DIT_GEMM_SINGLE_CTA=1
+ * projections on single CTAs instead of CTA pairs; H3DIT_GEMM_TAIL=0 no
+ * half tiles in a short last wave; H3DIT_GEMM_BAND=k raster bands of k
+ * N-tiles (default 16); H3DIT_DISABLE_GATED_ADALN=1 the gated residual and
+ * the following AdaLN as two launches. */
+
 /* ---------------------------------------------------------------- failure testing
  * Not part of the method (the pages have no counterpart); these let a test
  * drive the failure paths without faulting or hanging a GPU.
