@@ -63,19 +63,6 @@ struct AttnArgs {
   float scale_log2;
 };
 
-// O_i (+)= P_i V: A operand (P, 128 rows x 16 keys per MMA) read from TMEM.
-__device__ __forceinline__ void tc_mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                               uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n"
-      " .reg .pred p;\n"
-      " setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
-      "}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 template <int DH>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -174,25 +161,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // ---------------- MMA issuer
       constexpr uint32_t id_s = idesc_bf16_f32(kAttnBQ, kAttnBKV);
       constexpr uint32_t id_o = idesc_bf16_f32(kAttnBQ, DH);
-      const uint32_t sq = smem_u32(smem + L::kQOff);
+      // operand descriptors as their low words (start address >> 4 plus
+      // offsets; the high word is the same for all of them)
+      const uint32_t q_lo = sdesc_lo(smem_u32(smem + L::kQOff));
+      const uint32_t k_lo = sdesc_lo(smem_u32(smem + L::kKOff));
+      const uint32_t v_lo = sdesc_lo(smem_u32(smem + L::kVOff));
       auto issue_s = [&](int i, int j) {
-        const uint32_t sk = smem_u32(smem + L::kKOff + (j & 1) * L::kKBytes);
-        const uint32_t sqi = sq + i * L::kQBytes;
+        const uint32_t ka = k_lo + (j & 1) * (L::kKBytes >> 4);
+        const uint32_t qa = q_lo + i * (L::kQBytes >> 4);
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (kAttnBQ * 128) + (kk & 3) * 32;
-          const uint32_t offk = (kk >> 2) * (kAttnBKV * 128) + (kk & 3) * 32;
-          tc_mma_bf16(tmem_base + i * kAttnBKV, sdesc_k128(sqi + off), sdesc_k128(sk + offk), id_s, kk != 0);
+          const uint32_t off = ((kk >> 2) * (kAttnBQ * 128) + (kk & 3) * 32) >> 4;
+          const uint32_t offk = ((kk >> 2) * (kAttnBKV * 128) + (kk & 3) * 32) >> 4;
+          tc_mma_ss_lo(tmem_base + i * kAttnBKV, qa + off, ka + offk, id_s, kk != 0);
         }
         tc_commit(b_sfull + 8 * i);
       };
       auto issue_pv = [&](int i, int j) {
-        const uint32_t sv = smem_u32(smem + L::kVOff + (j & 1) * L::kVBytes);
+        const uint32_t va = v_lo + (j & 1) * (L::kVBytes >> 4);
 #pragma unroll
         for (int kk = 0; kk < kAttnBKV / 16; ++kk) {
-          const uint32_t offv = (kk >> 2) * (DH * 128) + (kk & 3) * 32;
-          tc_mma_bf16_ts(tmem_base + 256 + i * DH, tmem_base + i * kAttnBKV + kk * 8, sdesc_k128(sv + offv),
-                         id_o, (j | kk) != 0);
+          const uint32_t offv = ((kk >> 2) * (DH * 128) + (kk & 3) * 32) >> 4;
+          tc_mma_ts_lo(tmem_base + 256 + i * DH, tmem_base + i * kAttnBKV + kk * 8, va + offv, id_o, (j | kk) != 0);
         }
       };
       bool ok = mbar_wait(b_qfull, 0, abort_flag) && mbar_wait(b_kfull, 0, abort_flag);

@@ -247,6 +247,21 @@ __device__ __forceinline__ void tc_mma_ss_lo(uint32_t d_tmem, uint32_t a_lo, uin
       : "memory");
 }
 
+// D(tmem) (+)= A(tmem) * B^T, B in shared memory given its low descriptor word.
+__device__ __forceinline__ void tc_mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " .reg .b64 db;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " mov.b64 db, {%2, %5};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHi)
+      : "memory");
+}
+
 // 32 consecutive fp32 columns of this warp's 32 TMEM lanes (one lane per
 // thread), loaded and waited for in one statement so no use of the
 // registers can be scheduled ahead of the wait.
