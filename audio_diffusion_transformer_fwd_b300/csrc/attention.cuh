@@ -169,20 +169,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       auto issue_s = [&](int i, int j) {
         const uint32_t ka = k_lo + (j & 1) * (L::kKBytes >> 4);
         const uint32_t qa = q_lo + i * (L::kQBytes >> 4);
+        if constexpr (DH == 128) {
+          tc_mma_ss_k128(tmem_base + i * kAttnBKV, qa, ka, id_s, 0);
+        } else {
 #pragma unroll
-        for (int kk = 0; kk < DH / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * (kAttnBQ * 128) + (kk & 3) * 32) >> 4;
-          const uint32_t offk = ((kk >> 2) * (kAttnBKV * 128) + (kk & 3) * 32) >> 4;
-          tc_mma_ss_lo(tmem_base + i * kAttnBKV, qa + off, ka + offk, id_s, kk != 0);
+          for (int kk = 0; kk < DH / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * (kAttnBQ * 128) + (kk & 3) * 32) >> 4;
+            const uint32_t offk = ((kk >> 2) * (kAttnBKV * 128) + (kk & 3) * 32) >> 4;
+            tc_mma_ss_lo(tmem_base + i * kAttnBKV, qa + off, ka + offk, id_s, kk != 0);
+          }
         }
         tc_commit(b_sfull + 8 * i);
       };
       auto issue_pv = [&](int i, int j) {
         const uint32_t va = v_lo + (j & 1) * (L::kVBytes >> 4);
+        if constexpr (DH == 128) {
+          tc_mma_ts_k128(tmem_base + 256 + i * DH, tmem_base + i * kAttnBKV, va, id_o, j != 0);
+        } else {
 #pragma unroll
-        for (int kk = 0; kk < kAttnBKV / 16; ++kk) {
-          const uint32_t offv = ((kk >> 2) * (DH * 128) + (kk & 3) * 32) >> 4;
-          tc_mma_ts_lo(tmem_base + 256 + i * DH, tmem_base + i * kAttnBKV + kk * 8, va + offv, id_o, (j | kk) != 0);
+          for (int kk = 0; kk < kAttnBKV / 16; ++kk) {
+            const uint32_t offv = ((kk >> 2) * (DH * 128) + (kk & 3) * 32) >> 4;
+            tc_mma_ts_lo(tmem_base + 256 + i * DH, tmem_base + i * kAttnBKV + kk * 8, va + offv, id_o,
+                         (j | kk) != 0);
+          }
         }
       };
       bool ok = mbar_wait(b_qfull, 0, abort_flag) && mbar_wait(b_kfull, 0, abort_flag);

@@ -262,6 +262,110 @@ __device__ __forceinline__ void tc_mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
+// Eight MMAs over one 128-deep K extent of K-major operands in the 128-byte
+// swizzle (two blocks of 64 columns, 16 KB apart for 128 rows): operand k
+// starts 32 bytes (low-word step 2) after operand k-1 within a block and
+// 1024 low-word units later in the second block.  The first MMA accumulates
+// if `acc` is non-zero, the other seven always.  One asm statement, so the
+// issuing thread spends no instructions re-deriving the predicate and the
+// 64-bit descriptors between the MMAs.
+__device__ __forceinline__ void tc_mma_ss_k128(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                               uint32_t acc) {
+  asm volatile(
+      "{\n"
+      " .reg .pred p, t;\n"
+      " .reg .b64 da, db;\n"
+      " .reg .b32 a, b;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " setp.eq.b32 t, %4, %4;\n"
+      " mov.b64 da, {%1, %5};\n"
+      " mov.b64 db, {%2, %5};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n"
+      " add.u32 a, %1, 2;\n"
+      " add.u32 b, %2, 2;\n"
+      " mov.b64 da, {a, %5};\n"
+      " mov.b64 db, {b, %5};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, t;\n"
+      " add.u32 a, %1, 4;\n"
+      " add.u32 b, %2, 4;\n"
+      " mov.b64 da, {a, %5};\n"
+      " mov.b64 db, {b, %5};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, t;\n"
+      " add.u32 a, %1, 6;\n"
+      " add.u32 b, %2, 6;\n"
+      " mov.b64 da, {a, %5};\n"
+      " mov.b64 db, {b, %5};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, t;\n"
+      " add.u32 a, %1, 1024;\n"
+      " add.u32 b, %2, 1024;\n"
+      " mov.b64 da, {a, %5};\n"
+      " mov.b64 db, {b, %5};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, t;\n"
+      " add.u32 a, %1, 1026;\n"
+      " add.u32 b, %2, 1026;\n"
+      " mov.b64 da, {a, %5};\n"
+      " mov.b64 db, {b, %5};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, t;\n"
+      " add.u32 a, %1, 1028;\n"
+      " add.u32 b, %2, 1028;\n"
+      " mov.b64 da, {a, %5};\n"
+      " mov.b64 db, {b, %5};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, t;\n"
+      " add.u32 a, %1, 1030;\n"
+      " add.u32 b, %2, 1030;\n"
+      " mov.b64 da, {a, %5};\n"
+      " mov.b64 db, {b, %5};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, t;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(acc), "r"(kDescHi)
+      : "memory");
+}
+// The same with A read from tensor memory: operand k is 8 columns (16 BF16
+// keys as pairs) after operand k-1.
+__device__ __forceinline__ void tc_mma_ts_k128(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc,
+                                               uint32_t acc) {
+  asm volatile(
+      "{\n"
+      " .reg .pred p, t;\n"
+      " .reg .b64 db;\n"
+      " .reg .b32 a, b;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " setp.eq.b32 t, %4, %4;\n"
+      " mov.b64 db, {%2, %5};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n"
+      " add.u32 a, %1, 8;\n"
+      " add.u32 b, %2, 2;\n"
+      " mov.b64 db, {b, %5};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], db, %3, t;\n"
+      " add.u32 a, %1, 16;\n"
+      " add.u32 b, %2, 4;\n"
+      " mov.b64 db, {b, %5};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], db, %3, t;\n"
+      " add.u32 a, %1, 24;\n"
+      " add.u32 b, %2, 6;\n"
+      " mov.b64 db, {b, %5};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], db, %3, t;\n"
+      " add.u32 a, %1, 32;\n"
+      " add.u32 b, %2, 1024;\n"
+      " mov.b64 db, {b, %5};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], db, %3, t;\n"
+      " add.u32 a, %1, 40;\n"
+      " add.u32 b, %2, 1026;\n"
+      " mov.b64 db, {b, %5};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], db, %3, t;\n"
+      " add.u32 a, %1, 48;\n"
+      " add.u32 b, %2, 1028;\n"
+      " mov.b64 db, {b, %5};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], db, %3, t;\n"
+      " add.u32 a, %1, 56;\n"
+      " add.u32 b, %2, 1030;\n"
+      " mov.b64 db, {b, %5};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], db, %3, t;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(acc), "r"(kDescHi)
+      : "memory");
+}
+
 // 32 consecutive fp32 columns of this warp's 32 TMEM lanes (one lane per
 // thread), loaded and waited for in one statement so no use of the
 // registers can be scheduled ahead of the wait.
