@@ -61,6 +61,9 @@ struct AttnArgs {
   int heads;
   __nv_bfloat16* o;   // [n][heads*DH]
   float scale_log2;
+  int qpairs;     // 256-row query units per head
+  int unit0;      // first (head * qpairs + query unit) of this launch
+  int split;      // 1: CTA pairs share a unit, each taking half of the key tiles
 };
 
 template <int DH>
@@ -86,9 +89,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int q0 = blockIdx.x * (kAttnTilesQ * kAttnBQ);
-  const int head = blockIdx.y;
-  const int nkv = (args.n + kAttnBKV - 1) / kAttnBKV;
+  // work unit (head, 256 query rows); with split, the two CTAs of a cluster
+  // take key tiles [0, nkv/2) (rank 0) and [nkv/2, nkv) (rank 1) of it
+  const uint32_t rank = args.split ? cluster_ctarank() : 0u;
+  const int unit = args.unit0 + static_cast<int>(args.split ? (blockIdx.x >> 1) : blockIdx.x);
+  const int head = unit / args.qpairs;
+  const int q0 = (unit - head * args.qpairs) * (kAttnTilesQ * kAttnBQ);
+  const int nkv_all = (args.n + kAttnBKV - 1) / kAttnBKV;
+  const int jt0 = rank == 0 ? 0 : nkv_all / 2;                        // first key tile
+  const int nkv = args.split ? (rank == 0 ? nkv_all / 2 : nkv_all - nkv_all / 2) : nkv_all;   // key tiles here
 
   if (threadIdx.x == 0) {
     mbar_init(b_qfull, 1);
@@ -115,6 +124,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t tmem_base = *tmem_holder;
   // TMEM columns: S_0 (and P_0) at 0, S_1 (and P_1) at 128, O_0 at 256, O_1 at 256 + DH
   grid_dep_wait();
+  // a softmax thread's running max and sum at the end, for the split
+  // exchange; sm_ok: its key tiles and products all completed (warp-uniform)
+  float sm_m = -INFINITY, sm_l = 0.f;
+  bool sm_ok = false;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -139,14 +152,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         uint8_t* sk = smem + L::kKOff + st * L::kKBytes;
 #pragma unroll
         for (int a = 0; a < DH / 64; ++a)
-          tma_load_3d(smem_u32(sk + a * kAttnBKV * 128), &tmK, b_kfull + 8 * st, a * 64, j * kAttnBKV, head);
+          tma_load_3d(smem_u32(sk + a * kAttnBKV * 128), &tmK, b_kfull + 8 * st, a * 64, (jt0 + j) * kAttnBKV,
+                      head);
         ++issued_k;
         if (!mbar_wait(b_vempty + 8 * st, par, abort_flag)) { ok = false; break; }
         mbar_arrive_expect_tx(b_vfull + 8 * st, L::kVBytes);
         uint8_t* sv = smem + L::kVOff + st * L::kVBytes;
 #pragma unroll
         for (int a = 0; a < 2; ++a)
-          tma_load_3d(smem_u32(sv + a * DH * 128), &tmV, b_vfull + 8 * st, j * kAttnBKV + a * 64, 0, head);
+          tma_load_3d(smem_u32(sv + a * DH * 128), &tmV, b_vfull + 8 * st, (jt0 + j) * kAttnBKV + a * 64, 0,
+                      head);
         ++issued_v;
       }
       if (!ok) {
@@ -251,7 +266,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tc_fence_after();
       float s[kAttnBKV];
       tmem_ld128(t_s, s);
-      const int valid = args.n - j * kAttnBKV;
+      const int valid = args.n - (jt0 + j) * kAttnBKV;
       if (valid < kAttnBKV) {
 #pragma unroll
         for (int i = 0; i < kAttnBKV; ++i)
@@ -308,8 +323,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tc_fence_before();
       mbar_arrive(b_p);
     }
-    if (ok) {
-      if (mbar_wait(b_pvdone + 8 * ti, 0, abort_flag)) {
+    sm_ok = __all_sync(0xffffffffu, ok) && __all_sync(0xffffffffu, mbar_wait(b_pvdone + 8 * ti, 0, abort_flag));
+    sm_m = m_eff;
+    sm_l = l;
+    if (sm_ok && !args.split) {
+      {
         tc_fence_after();
         const int grow = q0 + ti * kAttnBQ + row;
         const float inv = 1.f / l;
@@ -326,6 +344,67 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
           }
+        }
+      }
+    }
+  }
+
+  if (args.split) {
+    // Combine the pair's halves of the keys: rank r finishes query tile r.
+    // Its partner sends the other tile's unnormalised O rows, running max
+    // and sum into r's shared memory (the K/V ring, idle now: both CTAs'
+    // copies and products have completed before the first cluster barrier),
+    // O as float4 [DH / 4][128 rows] so that a warp's stores are contiguous,
+    // then m[128] and l[128].
+    float* xo = reinterpret_cast<float*>(smem + L::kKOff);
+    const int ti = (warp - 4) >> 2;
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t t_o = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 256 + ti * DH;
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync_all();
+    tc_fence_after();
+    if (warp >= 4 && ti != static_cast<int>(rank) && sm_ok) {
+      const uint32_t dst = mapa_shared(smem_u32(xo), rank ^ 1u);
+#pragma unroll 1
+      for (int cc = 0; cc < DH / 32; ++cc) {
+        float v[32];
+        tmem_ld32(t_o + cc * 32, v);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          st_cluster_f4(dst + ((cc * 8 + q) * kAttnBQ + row) * 16, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      }
+      st_cluster_f32(dst + (DH * kAttnBQ + row) * 4, sm_m);
+      st_cluster_f32(dst + (DH * kAttnBQ + kAttnBQ + row) * 4, sm_l);
+    }
+    __syncwarp();
+    cluster_sync_all();
+    if (warp >= 4 && ti == static_cast<int>(rank) && sm_ok) {
+      const float m1 = xo[DH * kAttnBQ + row];
+      const float l1 = xo[DH * kAttnBQ + kAttnBQ + row];
+      const float m = fmaxf(sm_m, m1);
+      const float a0 = fast_exp2(sm_m - m), a1 = fast_exp2(m1 - m);
+      const float inv = 1.f / (sm_l * a0 + l1 * a1);
+      const float4* o1 = reinterpret_cast<const float4*>(xo);
+      const int grow = q0 + ti * kAttnBQ + row;
+      const int d = args.heads * DH;
+#pragma unroll 1
+      for (int cc = 0; cc < DH / 32; ++cc) {
+        float v[32];
+        tmem_ld32(t_o + cc * 32, v);
+        if (grow < args.n) {
+          uint32_t p[16];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 w = o1[(cc * 8 + q) * kAttnBQ + row];
+            const float y0 = (v[4 * q] * a0 + w.x * a1) * inv, y1 = (v[4 * q + 1] * a0 + w.y * a1) * inv;
+            const float y2 = (v[4 * q + 2] * a0 + w.z * a1) * inv, y3 = (v[4 * q + 3] * a0 + w.w * a1) * inv;
+            p[2 * q] = pack_bf16x2(y0, y1);
+            p[2 * q + 1] = pack_bf16x2(y2, y3);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(args.o + static_cast<size_t>(grow) * d + head * DH + cc * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
         }
       }
     }

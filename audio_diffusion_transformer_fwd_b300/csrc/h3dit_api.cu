@@ -599,6 +599,13 @@ h3dit_status launch_gemm_i8(int epi, const void* A, const float* sa, int group, 
   }
 }
 
+// The key split of a short last wave of attention units (default;
+// H3DIT_ATTN_SPLIT=0 runs whole units only: an A/B switch read at every call).
+bool attn_split_enabled() {
+  const char* e = getenv("H3DIT_ATTN_SPLIT");
+  return !(e && e[0] == '0');
+}
+
 h3dit_status launch_attention(const h3dit_config* c, const void* q, const void* k, const void* vt, int vt_ld,
                               int n, void* o, cudaStream_t s) {
   const int dh = c->head_dim, H = c->heads;
@@ -624,19 +631,34 @@ h3dit_status launch_attention(const h3dit_config* c, const void* q, const void* 
   a.heads = H;
   a.o = static_cast<bf16*>(o);
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)dh);
+  // One CTA (one per SM: its shared memory) per unit of 256 query rows of a
+  // head.  When the last wave of units would keep at most half of the SMs
+  // busy, those units run as CTA pairs that split the keys in two and
+  // combine their partial results, so the tail takes about half a wave.
   const int rows_per_cta = h3::kAttnTilesQ * h3::kAttnBQ;
-  dim3 grid((n + rows_per_cta - 1) / rows_per_cta, H);
+  a.qpairs = (n + rows_per_cta - 1) / rows_per_cta;
+  const long long units = 1LL * a.qpairs * H;
+  if (units > 0x3fffffffLL) return fail(H3DIT_E_UNSUPPORTED, "attention: %lld units", units);
+  const int nkv = (n + h3::kAttnBKV - 1) / h3::kAttnBKV;
+  const int sms = sm_count();
+  const int rem = static_cast<int>(units % sms);
+  const int tail = (attn_split_enabled() && units > sms && rem > 0 && 2 * rem <= sms && nkv >= 2) ? rem : 0;
+  const int full = static_cast<int>(units) - tail;
   TimedLaunch tl(kAttn, s);
-  if (dh == 128) {
-    H3_TRY(set_smem(h3::attn_fwd_tc_kernel<128>, h3::AttnSmem<128>::kTotal));
-    H3_TRY(launch_ex(h3::attn_fwd_tc_kernel<128>, grid, dim3(h3::kAttnThreads), h3::AttnSmem<128>::kTotal, s, 1,
-                     tq, tk, tv, a));
-  } else {
-    H3_TRY(set_smem(h3::attn_fwd_tc_kernel<64>, h3::AttnSmem<64>::kTotal));
-    H3_TRY(launch_ex(h3::attn_fwd_tc_kernel<64>, grid, dim3(h3::kAttnThreads), h3::AttnSmem<64>::kTotal, s, 1,
-                     tq, tk, tv, a));
-  }
-  H3_CUDA(cudaGetLastError());
+  auto run = [&](auto kernel, size_t smem) -> h3dit_status {
+    H3_TRY(set_smem(kernel, smem));
+    a.unit0 = 0;
+    a.split = 0;
+    if (full > 0) H3_TRY(launch_ex(kernel, dim3(full), dim3(h3::kAttnThreads), smem, s, 1, tq, tk, tv, a));
+    if (tail > 0) {
+      a.unit0 = full;
+      a.split = 1;
+      H3_TRY(launch_ex(kernel, dim3(2 * tail), dim3(h3::kAttnThreads), smem, s, 2, tq, tk, tv, a));
+    }
+    return H3DIT_OK;
+  };
+  if (dh == 128) H3_TRY(run(h3::attn_fwd_tc_kernel<128>, h3::AttnSmem<128>::kTotal));
+  else H3_TRY(run(h3::attn_fwd_tc_kernel<64>, h3::AttnSmem<64>::kTotal));
   return H3DIT_OK;
 }
 

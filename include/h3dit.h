@@ -175,7 +175,10 @@ h3dit_status h3dit_check_device_error(cudaStream_t stream);
  * projections on single CTAs instead of CTA pairs; H3DIT_GEMM_TAIL=0 no
  * half tiles in a short last wave; H3DIT_GEMM_BAND=k raster bands of k
  * N-tiles (default 16); H3DIT_DISABLE_GATED_ADALN=1 the gated residual and
- * the following AdaLN as two launches. */
+ * the following AdaLN as two launches.  One switch changes rounding:
+ * H3DIT_ATTN_SPLIT=0 runs the attention units of a short last wave whole,
+ * instead of as CTA pairs that each take half of the keys and combine their
+ * partial results (the same softmax; the combine rounds differently). */
 
 /* ---------------------------------------------------------------- failure testing
  * Not part of the method (the pages have no counterpart); these let a test

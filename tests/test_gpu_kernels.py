@@ -333,3 +333,38 @@ def test_qkv_projection_tail_halves_equal_whole_tiles(monkeypatch):
     for x, y in zip(*outs):
         assert torch.equal(x, y)
         assert not torch.isnan(x.float()).any()
+
+
+@pytest.mark.parametrize("heads,dh,n", [(40, 128, 1100), (64, 64, 600)])
+def test_attention_split_tail_units(monkeypatch, heads, dh, n):
+    """More 256-row units than SMs with a short last wave (200 units for
+    40 heads x 1100 tokens; 192 for 64 x 600): the last wave's units run as
+    CTA pairs that split the keys in two and combine (O, running max, row
+    sum) through distributed shared memory.  Every output is written and
+    follows the oracle; against whole units (H3DIT_ATTN_SPLIT=0) only the
+    combine's rounding differs (within one BF16 step of the output)."""
+    shape = H.BlockShape(heads * dh, heads, dh, 256, rope_sections=(dh // 4, 3 * dh // 8, 3 * dh // 8))
+    r = np.random.default_rng(900 + n)
+    q = synth.to_bf16_values(r.standard_normal((heads, n, dh)).astype(np.float32) * 1.5)
+    k = synth.to_bf16_values(r.standard_normal((heads, n, dh)).astype(np.float32) * 1.5)
+    v = synth.to_bf16_values(r.standard_normal((heads, n, dh)).astype(np.float32))
+    vt_ld = (n + 63) // 64 * 64
+    vt = np.zeros((heads, dh, vt_ld), np.float32)
+    vt[:, :, :n] = v.transpose(0, 2, 1)
+    qd, kd, vd = dev_bf16(q), dev_bf16(k), dev_bf16(vt)
+    outs = []
+    for split in ("1", "0"):
+        monkeypatch.setenv("H3DIT_ATTN_SPLIT", split)
+        o = torch.full((n, heads * dh), float("nan"), device="cuda", dtype=torch.bfloat16)
+        H.h3dit_attention(shape, qd, kd, vd, vt_ld, n, o)
+        H.h3dit_check_device_error()
+        outs.append(host(o))
+    assert not np.isnan(outs[0]).any()
+    ref = O.attention(q, k, v).transpose(1, 0, 2).reshape(n, heads * dh)
+    for got in outs:
+        _close(got, ref, rel=1e-2, amax_frac=2.0 ** -6)
+    a, b = outs
+    diff = np.abs(a - b)
+    i = np.unravel_index(np.argmax(diff), diff.shape)
+    assert rel_l2(a, b) <= 2e-3 and diff.max() <= 2.0 ** -7 * float(np.max(np.abs(b))), \
+        f"rel_l2 {rel_l2(a, b):.3e}, max diff {diff.max():.3e} at {i}: {a[i]} vs {b[i]}, max|o| {np.max(np.abs(b)):.3e}"
