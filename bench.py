@@ -84,8 +84,9 @@ def write_traffic(csv_path):
     """profiles/ncu_traffic.json from an ncu --csv capture of
     dram__bytes_read.sum and dram__bytes_write.sum over the launches of one
     block (the command is in profiles/dram_traffic_block_512.md): DRAM bytes
-    per launch by kernel class, and the four GEMM launches' sum, stamped with
-    the hash of the kernel sources they were taken on."""
+    per launch by kernel class (attention: its launches of the block added),
+    and the four GEMM launches' sum, stamped with the hash of the kernel
+    sources they were taken on."""
     import csv
     import re
     scale = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1024.0, "MB": 1024.0 ** 2}
@@ -108,7 +109,10 @@ def write_traffic(csv_path):
         out["kernels"]["gemm_per_block"] = sum(b for _, b in gemms[:4])
     for name, b in per_launch.values():
         m = re.search(r"(attn_fwd|gate_adaln_kernel<[^>]*>|rope_table)", name)
-        if m:
+        if m and m.group(1) == "attn_fwd":
+            # the full waves and, when the last wave is short, its key-split tail
+            out["kernels"]["attn_fwd"] = out["kernels"].get("attn_fwd", 0.0) + b
+        elif m:
             out["kernels"].setdefault(m.group(1), b)
     with open(os.path.join(ROOT, "profiles", "ncu_traffic.json"), "w") as fh:
         json.dump(out, fh, indent=1)
