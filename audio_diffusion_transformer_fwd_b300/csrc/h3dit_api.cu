@@ -100,7 +100,7 @@ enum KernelClass { kRows = 0, kQKV = 1, kAttn = 2, kOProj = 3, kFC1 = 4, kFC2 = 
 struct Timing {
   std::mutex mu;
   bool enabled = false;
-  struct Pending { int cls; cudaEvent_t a, b; };
+  struct Pending { int cls; cudaEvent_t a, b; int kernels; };
   std::vector<Pending> pending;
   double total_ms[kNumClasses] = {0};
   long long count[kNumClasses] = {0};
@@ -110,6 +110,7 @@ struct TimedLaunch {
   int cls;
   cudaStream_t s;
   cudaEvent_t a = nullptr, b = nullptr;
+  int kernels = 1;   // kernel launches between the two events
   TimedLaunch(int c, cudaStream_t st) : cls(c), s(st) {
     if (!g_timing.enabled) return;
     cudaEventCreate(&a);
@@ -120,7 +121,7 @@ struct TimedLaunch {
     if (!a) return;
     cudaEventRecord(b, s);
     std::lock_guard<std::mutex> lk(g_timing.mu);
-    g_timing.pending.push_back({cls, a, b});
+    g_timing.pending.push_back({cls, a, b, kernels});
   }
 };
 
@@ -650,6 +651,7 @@ h3dit_status launch_attention(const h3dit_config* c, const void* q, const void* 
     a.unit0 = 0;
     a.split = 0;
     if (full > 0) H3_TRY(launch_ex(kernel, dim3(full), dim3(h3::kAttnThreads), smem, s, 1, tq, tk, tv, a));
+    tl.kernels = (full > 0 ? 1 : 0) + (tail > 0 ? 1 : 0);
     if (tail > 0) {
       a.unit0 = full;
       a.split = 1;
@@ -714,6 +716,7 @@ h3dit_status launch_rows(void* x, const void* branch, const float* gate, const f
     else
       H3_TRY(launch_row_kernel<true, true, false>(nv, xb, bb, gate, shift, scale, hb, nullptr, n, d, eps, sm, s));
   } else {
+    tl.kernels = (gate_on ? 1 : 0) + (norm_on ? 1 : 0);
     if (gate_on)
       H3_TRY(launch_row_kernel<true, false, false>(nv, xb, bb, gate, nullptr, nullptr, nullptr, nullptr, n, d, eps,
                                                    sm, s));
@@ -1033,7 +1036,7 @@ h3dit_status h3dit_timing_read(int cls, double* total_ms, long long* launches) {
     float ms = 0.f;
     H3_CUDA(cudaEventElapsedTime(&ms, p.a, p.b));
     g_timing.total_ms[p.cls] += ms;
-    g_timing.count[p.cls] += 1;
+    g_timing.count[p.cls] += p.kernels;
     cudaEventDestroy(p.a);
     cudaEventDestroy(p.b);
   }
@@ -1457,6 +1460,7 @@ h3dit_status h3dit_final_layer(const h3dit_config* cfg, const void* x, int n_tok
   ksplit = std::min(ksplit, d / h3::kHeadBK);
   hb.ksplit = ksplit;
   TimedLaunch tl(kRows, stream);
+  tl.kernels = 2;   // statistics, then the heads
   const long long stat_threads = (long long)hr.first_warp[n_heads] * 32;
   h3::head_stats_kernel<<<(unsigned)((stat_threads + 255) / 256), 256, 0, stream>>>(static_cast<const bf16*>(x), hr,
                                                                                     d, cfg->eps);

@@ -213,7 +213,7 @@ h3dit_status h3dit_test_stall_next_gemm(int kblock);
  * 0 row kernels, 1 QKV GEMM, 2 attention, 3 out-projection GEMM, 4 FC1 GEMM,
  * 5 FC2 GEMM, 6 token reduce/restore, 7 quantise.  h3dit_timing_read
  * synchronises the recorded events and returns the total milliseconds and
- * launch count of a class since the last reset. */
+ * the number of kernel launches of a class since the last reset. */
 h3dit_status h3dit_timing_enable(int on);
 h3dit_status h3dit_timing_reset(void);
 h3dit_status h3dit_timing_read(int kernel_class, double* total_ms, long long* launches);
