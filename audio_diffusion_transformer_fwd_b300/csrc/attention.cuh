@@ -32,7 +32,19 @@
 // Operands are K-major BF16 in the 128-byte swizzle: Q and K come from the
 // head-major [H][N][Dh] tensors, V from its transpose [H][Dh][ld] written by
 // the QKV epilogue.  Keys past N read as zeros (TMA bounds) and are masked
-// to probability 0; query rows past N are computed and not stored.
+// to probability 0; query rows past N are computed and not stored.  The
+// MMA thread's operands are descriptor low words advanced by constant
+// offsets (the high word is the same for all), and at Dh 128 each group of
+// eight MMAs is one asm statement: that thread's instruction count shows in
+// the kernel's speed.
+//
+// Work units are (head, 256 query rows), one CTA each.  A launch with
+// split = 1 runs each unit on a cluster of two CTAs instead, key tiles
+// [0, nkv/2) on rank 0 and the rest on rank 1, each with its own running
+// max and sum; at the end each CTA hands its partner the partner's query
+// tile (unnormalised O, max, sum) through distributed shared memory and
+// finishes its own tile (rank r: tile r) by the usual two-part combine.
+// The library uses it for the units of a short last wave.
 #pragma once
 #include "ptx.cuh"
 
