@@ -38,8 +38,12 @@
 // eight MMAs is one asm statement: that thread's instruction count shows in
 // the kernel's speed.
 //
-// Work units are (head, 256 query rows), one CTA each.  A launch with
-// split = 1 runs each unit on a cluster of two CTAs instead, key tiles
+// Work units are (head, 256 query rows).  A launch's CTAs are persistent:
+// each walks units first, first + grid, ... with every barrier phase
+// counting on, loading the next unit's query tiles (q_empty) while it
+// finishes the current one, and starting the next unit's products on O
+// once the epilogue has read it (o_free).  A launch with
+// split = 1 runs each of its units on a cluster of two CTAs instead, key tiles
 // [0, nkv/2) on rank 0 and the rest on rank 1, each with its own running
 // max and sum; at the end each CTA hands its partner the partner's query
 // tile (unnormalised O, max, sum) through distributed shared memory and
@@ -74,7 +78,8 @@ struct AttnArgs {
   __nv_bfloat16* o;   // [n][heads*DH]
   float scale_log2;
   int qpairs;     // 256-row query units per head
-  int unit0;      // first (head * qpairs + query unit) of this launch
+  int unit0;      // first unit (head * qpairs + query unit) of this launch
+  int units;      // units of this launch; a CTA (or CTA pair) walks unit0 + first + k * stride
   int split;      // 1: CTA pairs share a unit, each taking half of the key tiles
 };
 
@@ -86,33 +91,39 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
-  // bars: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done[2], drain
+  // bars: q_full, q_empty, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done[2],
+  // o_free[2], drain
   const uint32_t b_qfull = smem_u32(bars + 0);
-  const uint32_t b_kfull = smem_u32(bars + 1);
-  const uint32_t b_kempty = smem_u32(bars + 3);
-  const uint32_t b_vfull = smem_u32(bars + 5);
-  const uint32_t b_vempty = smem_u32(bars + 7);
-  const uint32_t b_sfull = smem_u32(bars + 9);
-  const uint32_t b_pfull = smem_u32(bars + 11);
-  const uint32_t b_pvdone = smem_u32(bars + 13);
-  const uint32_t b_drain = smem_u32(bars + 15);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 16);
+  const uint32_t b_qempty = smem_u32(bars + 1);
+  const uint32_t b_kfull = smem_u32(bars + 2);
+  const uint32_t b_kempty = smem_u32(bars + 4);
+  const uint32_t b_vfull = smem_u32(bars + 6);
+  const uint32_t b_vempty = smem_u32(bars + 8);
+  const uint32_t b_sfull = smem_u32(bars + 10);
+  const uint32_t b_pfull = smem_u32(bars + 12);
+  const uint32_t b_pvdone = smem_u32(bars + 14);
+  const uint32_t b_ofree = smem_u32(bars + 16);
+  const uint32_t b_drain = smem_u32(bars + 18);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 19);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // work unit (head, 256 query rows); with split, the two CTAs of a cluster
-  // take key tiles [0, nkv/2) (rank 0) and [nkv/2, nkv) (rank 1) of it
+  // Units (head, 256 query rows): this CTA (pair) takes unit0 + first,
+  // + stride, ...; every barrier phase below counts on across units.  With
+  // split, the two CTAs of a cluster share one unit: key tiles [0, nkv/2)
+  // on rank 0, the rest on rank 1.
   const uint32_t rank = args.split ? cluster_ctarank() : 0u;
-  const int unit = args.unit0 + static_cast<int>(args.split ? (blockIdx.x >> 1) : blockIdx.x);
-  const int head = unit / args.qpairs;
-  const int q0 = (unit - head * args.qpairs) * (kAttnTilesQ * kAttnBQ);
+  const int first = static_cast<int>(args.split ? (blockIdx.x >> 1) : blockIdx.x);
+  const int stride = static_cast<int>(args.split ? (gridDim.x >> 1) : gridDim.x);
+  const int my_units = first < args.units ? (args.units - first + stride - 1) / stride : 0;
   const int nkv_all = (args.n + kAttnBKV - 1) / kAttnBKV;
   const int jt0 = rank == 0 ? 0 : nkv_all / 2;                        // first key tile
   const int nkv = args.split ? (rank == 0 ? nkv_all / 2 : nkv_all - nkv_all / 2) : nkv_all;   // key tiles here
 
   if (threadIdx.x == 0) {
     mbar_init(b_qfull, 1);
+    mbar_init(b_qempty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_kfull + 8 * i, 1);
       mbar_init(b_kempty + 8 * i, 1);
@@ -121,6 +132,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(b_sfull + 8 * i, 1);
       mbar_init(b_pfull + 8 * i, 128);
       mbar_init(b_pvdone + 8 * i, 1);
+      mbar_init(b_ofree + 8 * i, 128);
     }
     mbar_init(b_drain, 1);
     *abort_flag = 0;
@@ -136,51 +148,62 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t tmem_base = *tmem_holder;
   // TMEM columns: S_0 (and P_0) at 0, S_1 (and P_1) at 128, O_0 at 256, O_1 at 256 + DH
   grid_dep_wait();
-  // a softmax thread's running max and sum at the end, for the split
-  // exchange; sm_ok: its key tiles and products all completed (warp-uniform)
+  // a softmax thread's running max and sum at the end of its (one) unit,
+  // for the split exchange; sm_ok: that unit's key tiles and products all
+  // completed (warp-uniform)
   float sm_m = -INFINITY, sm_l = 0.f;
   bool sm_ok = false;
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer
+      // ---------------- TMA producer: per unit its two query tiles, then
+      // its key and V^T tiles through the two-stage rings (global count g)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(b_qfull, kAttnTilesQ * L::kQBytes);
-#pragma unroll
-      for (int i = 0; i < kAttnTilesQ; ++i)
-#pragma unroll
-        for (int a = 0; a < DH / 64; ++a)
-          tma_load_3d(smem_u32(smem + L::kQOff + i * L::kQBytes + a * kAttnBQ * 128), &tmQ, b_qfull, a * 64,
-                      q0 + i * kAttnBQ, head);
-      int issued_k = 0, issued_v = 0;
+      int issued_k = 0, issued_v = 0, issued_q = 0;
       bool ok = true;
-      for (int j = 0; j < nkv && ok; ++j) {
-        const int st = j & 1;
-        const uint32_t par = ((j >> 1) & 1) ^ 1;
-        if (!mbar_wait(b_kempty + 8 * st, par, abort_flag)) { ok = false; break; }
-        mbar_arrive_expect_tx(b_kfull + 8 * st, L::kKBytes);
-        uint8_t* sk = smem + L::kKOff + st * L::kKBytes;
+      for (int k = 0; k < my_units && ok; ++k) {
+        const int unit = args.unit0 + first + k * stride;
+        const int head = unit / args.qpairs;
+        const int q0 = (unit - head * args.qpairs) * (kAttnTilesQ * kAttnBQ);
+        // the previous unit's S products have all read its query tiles
+        if (k > 0 && !mbar_wait(b_qempty, (k - 1) & 1, abort_flag)) { ok = false; break; }
+        mbar_arrive_expect_tx(b_qfull, kAttnTilesQ * L::kQBytes);
 #pragma unroll
-        for (int a = 0; a < DH / 64; ++a)
-          tma_load_3d(smem_u32(sk + a * kAttnBKV * 128), &tmK, b_kfull + 8 * st, a * 64, (jt0 + j) * kAttnBKV,
-                      head);
-        ++issued_k;
-        if (!mbar_wait(b_vempty + 8 * st, par, abort_flag)) { ok = false; break; }
-        mbar_arrive_expect_tx(b_vfull + 8 * st, L::kVBytes);
-        uint8_t* sv = smem + L::kVOff + st * L::kVBytes;
+        for (int i = 0; i < kAttnTilesQ; ++i)
 #pragma unroll
-        for (int a = 0; a < 2; ++a)
-          tma_load_3d(smem_u32(sv + a * DH * 128), &tmV, b_vfull + 8 * st, (jt0 + j) * kAttnBKV + a * 64, 0,
-                      head);
-        ++issued_v;
+          for (int a = 0; a < DH / 64; ++a)
+            tma_load_3d(smem_u32(smem + L::kQOff + i * L::kQBytes + a * kAttnBQ * 128), &tmQ, b_qfull, a * 64,
+                        q0 + i * kAttnBQ, head);
+        ++issued_q;
+        for (int j = 0; j < nkv; ++j) {
+          const int g = k * nkv + j;
+          const int st = g & 1;
+          const uint32_t par = ((g >> 1) & 1) ^ 1;
+          if (!mbar_wait(b_kempty + 8 * st, par, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(b_kfull + 8 * st, L::kKBytes);
+          uint8_t* sk = smem + L::kKOff + st * L::kKBytes;
+#pragma unroll
+          for (int a = 0; a < DH / 64; ++a)
+            tma_load_3d(smem_u32(sk + a * kAttnBKV * 128), &tmK, b_kfull + 8 * st, a * 64, (jt0 + j) * kAttnBKV,
+                        head);
+          ++issued_k;
+          if (!mbar_wait(b_vempty + 8 * st, par, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(b_vfull + 8 * st, L::kVBytes);
+          uint8_t* sv = smem + L::kVOff + st * L::kVBytes;
+#pragma unroll
+          for (int a = 0; a < 2; ++a)
+            tma_load_3d(smem_u32(sv + a * DH * 128), &tmV, b_vfull + 8 * st, (jt0 + j) * kAttnBKV + a * 64, 0,
+                        head);
+          ++issued_v;
+        }
       }
       if (!ok) {
         // let the loads still in flight land before the CTA exits
-        for (int j = max(0, issued_k - 2); j < issued_k; ++j) mbar_wait_drain(b_kfull + 8 * (j & 1), (j >> 1) & 1);
-        for (int j = max(0, issued_v - 2); j < issued_v; ++j) mbar_wait_drain(b_vfull + 8 * (j & 1), (j >> 1) & 1);
-        mbar_wait_drain(b_qfull, 0);
+        for (int g = max(0, issued_k - 2); g < issued_k; ++g) mbar_wait_drain(b_kfull + 8 * (g & 1), (g >> 1) & 1);
+        for (int g = max(0, issued_v - 2); g < issued_v; ++g) mbar_wait_drain(b_vfull + 8 * (g & 1), (g >> 1) & 1);
+        if (issued_q > 0) mbar_wait_drain(b_qfull, (issued_q - 1) & 1);
       }
     }
   } else if (warp == 1) {
@@ -193,8 +216,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const uint32_t q_lo = sdesc_lo(smem_u32(smem + L::kQOff));
       const uint32_t k_lo = sdesc_lo(smem_u32(smem + L::kKOff));
       const uint32_t v_lo = sdesc_lo(smem_u32(smem + L::kVOff));
-      auto issue_s = [&](int i, int j) {
-        const uint32_t ka = k_lo + (j & 1) * (L::kKBytes >> 4);
+      auto issue_s = [&](int i, int g) {
+        const uint32_t ka = k_lo + (g & 1) * (L::kKBytes >> 4);
         const uint32_t qa = q_lo + i * (L::kQBytes >> 4);
         if constexpr (DH == 128) {
           tc_mma_ss_k128(tmem_base + i * kAttnBKV, qa, ka, id_s, 0);
@@ -208,51 +231,63 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         tc_commit(b_sfull + 8 * i);
       };
-      auto issue_pv = [&](int i, int j) {
-        const uint32_t va = v_lo + (j & 1) * (L::kVBytes >> 4);
+      auto issue_pv = [&](int i, int g, bool acc) {
+        const uint32_t va = v_lo + (g & 1) * (L::kVBytes >> 4);
         if constexpr (DH == 128) {
-          tc_mma_ts_k128(tmem_base + 256 + i * DH, tmem_base + i * kAttnBKV, va, id_o, j != 0);
+          tc_mma_ts_k128(tmem_base + 256 + i * DH, tmem_base + i * kAttnBKV, va, id_o, acc);
         } else {
 #pragma unroll
           for (int kk = 0; kk < kAttnBKV / 16; ++kk) {
             const uint32_t offv = ((kk >> 2) * (DH * 128) + (kk & 3) * 32) >> 4;
             tc_mma_ts_lo(tmem_base + 256 + i * DH, tmem_base + i * kAttnBKV + kk * 8, va + offv, id_o,
-                         (j | kk) != 0);
+                         acc || kk != 0);
           }
         }
       };
-      bool ok = mbar_wait(b_qfull, 0, abort_flag) && mbar_wait(b_kfull, 0, abort_flag);
-      if (ok) {
+      bool ok = true;
+      for (int k = 0; k < my_units && ok; ++k) {
+        const int base = k * nkv;
+        if (!mbar_wait(b_qfull, k & 1, abort_flag) || !mbar_wait(b_kfull + 8 * (base & 1), (base >> 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        issue_s(0, 0);
-        issue_s(1, 0);
-        tc_commit(b_kempty);
-      }
-      for (int j = 0; j < nkv && ok; ++j) {
-        const int st = j & 1;
-        const uint32_t par = (j >> 1) & 1;
-        const bool more = j + 1 < nkv;
-        if (!mbar_wait(b_vfull + 8 * st, par, abort_flag)) { ok = false; break; }
-        // tile 0: O_0 += P_0 V_j, then S_0 of the next key tile
-        if (!mbar_wait(b_pfull, j & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        issue_pv(0, j);
-        if (more) {
-          if (!mbar_wait(b_kfull + 8 * ((j + 1) & 1), ((j + 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+        issue_s(0, base);
+        issue_s(1, base);
+        tc_commit(b_kempty + 8 * (base & 1));
+        // a unit's first products overwrite O_0 / O_1, which the previous
+        // unit's epilogue must have read (waited for before the loop, so
+        // that the per-tile loop stays as lean as in a single-unit CTA)
+        if (k > 0 && (!mbar_wait(b_ofree, (k - 1) & 1, abort_flag) || !mbar_wait(b_ofree + 8, (k - 1) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        for (int j = 0; j < nkv; ++j) {
+          const int g = base + j;
+          const int st = g & 1;
+          const bool more = j + 1 < nkv;
+          if (!mbar_wait(b_vfull + 8 * st, (g >> 1) & 1, abort_flag)) { ok = false; break; }
+          // tile 0: O_0 += P_0 V_j, then S_0 of the next key tile
+          if (!mbar_wait(b_pfull, g & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          issue_s(0, j + 1);
+          issue_pv(0, g, j != 0);
+          if (more) {
+            if (!mbar_wait(b_kfull + 8 * ((g + 1) & 1), ((g + 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(0, g + 1);
+          }
+          // tile 1
+          if (!mbar_wait(b_pfull + 8, g & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(1, g, j != 0);
+          tc_commit(b_vempty + 8 * st);
+          if (more) {
+            issue_s(1, g + 1);
+            tc_commit(b_kempty + 8 * ((g + 1) & 1));
+          }
         }
-        // tile 1
-        if (!mbar_wait(b_pfull + 8, j & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        issue_pv(1, j);
-        tc_commit(b_vempty + 8 * st);
-        if (more) {
-          issue_s(1, j + 1);
-          tc_commit(b_kempty + 8 * ((j + 1) & 1));
-        }
-      }
-      if (ok) {
+        if (!ok) break;
+        tc_commit(b_qempty);   // every S product of the unit is complete with it
         tc_commit(b_pvdone);
         tc_commit(b_pvdone + 8);
       }
@@ -270,76 +305,81 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t b_s = b_sfull + 8 * ti;
     const uint32_t b_p = b_pfull + 8 * ti;
     const float c = args.scale_log2;
-    float m_eff = -INFINITY;
-    float l = 0.f;
     bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      if (!mbar_wait(b_s, j & 1, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      float s[kAttnBKV];
-      tmem_ld128(t_s, s);
-      const int valid = args.n - (jt0 + j) * kAttnBKV;
-      if (valid < kAttnBKV) {
+    for (int k = 0; k < my_units && ok; ++k) {
+      const int unit = args.unit0 + first + k * stride;
+      const int head = unit / args.qpairs;
+      const int q0 = (unit - head * args.qpairs) * (kAttnTilesQ * kAttnBQ);
+      float m_eff = -INFINITY;
+      float l = 0.f;
+      for (int j = 0; j < nkv; ++j) {
+        const int g = k * nkv + j;
+        if (!mbar_wait(b_s, g & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        float s[kAttnBKV];
+        tmem_ld128(t_s, s);
+        const int valid = args.n - (jt0 + j) * kAttnBKV;
+        if (valid < kAttnBKV) {
 #pragma unroll
-        for (int i = 0; i < kAttnBKV; ++i)
-          if (i >= valid) s[i] = -INFINITY;
-      }
-      float mx4[4] = {s[0], s[1], s[2], s[3]};
-#pragma unroll
-      for (int i = 4; i < kAttnBKV - 4; i += 8) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) mx4[e] = fmax3(mx4[e], s[i + 2 * e], s[i + 2 * e + 1]);
-      }
-      const float mx = fmax3(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]),
-                             fmax3(s[kAttnBKV - 4], s[kAttnBKV - 3], fmaxf(s[kAttnBKV - 2], s[kAttnBKV - 1]))) * c;
-      float alpha = 1.f;
-      bool rescale = false;
-      if (j == 0) {
-        m_eff = mx;
-      } else if (mx > m_eff + kAttnRescaleLog2) {
-        alpha = fast_exp2(m_eff - mx);
-        m_eff = mx;
-        rescale = true;
-      }
-      const float neg_m = -m_eff;
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // 4 packed partial sums
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int i = half * 64 + 2 * e;
-          float x0, x1;
-          ffma2(x0, x1, s[i], s[i + 1], c, c, neg_m, neg_m);
-          const float p0 = fast_exp2(x0);
-          const float p1 = fast_exp2(x1);
-          const int a = 2 * (e & 3);
-          fadd2(acc[a], acc[a + 1], acc[a], acc[a + 1], p0, p1);
-          pk[e] = pack_bf16x2(p0, p1);
+          for (int i = 0; i < kAttnBKV; ++i)
+            if (i >= valid) s[i] = -INFINITY;
         }
-        tmem_st32u(t_s + half * 32, pk);
-      }
-      l = l * alpha + (((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7])));
-      // O_i holds the products up to key tile j-1 (complete: S_i(j) was
-      // issued after them); rescale it to the new max before PV_i(j).
-      if (__any_sync(0xffffffffu, rescale)) {
+        float mx4[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+        for (int i = 4; i < kAttnBKV - 4; i += 8) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) mx4[e] = fmax3(mx4[e], s[i + 2 * e], s[i + 2 * e + 1]);
+        }
+        const float mx = fmax3(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]),
+                               fmax3(s[kAttnBKV - 4], s[kAttnBKV - 3], fmaxf(s[kAttnBKV - 2], s[kAttnBKV - 1]))) * c;
+        float alpha = 1.f;
+        bool rescale = false;
+        if (j == 0) {
+          m_eff = mx;
+        } else if (mx > m_eff + kAttnRescaleLog2) {
+          alpha = fast_exp2(m_eff - mx);
+          m_eff = mx;
+          rescale = true;
+        }
+        const float neg_m = -m_eff;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // 4 packed partial sums
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int i = half * 64 + 2 * e;
+            float x0, x1;
+            ffma2(x0, x1, s[i], s[i + 1], c, c, neg_m, neg_m);
+            const float p0 = fast_exp2(x0);
+            const float p1 = fast_exp2(x1);
+            const int a = 2 * (e & 3);
+            fadd2(acc[a], acc[a + 1], acc[a], acc[a + 1], p0, p1);
+            pk[e] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32u(t_s + half * 32, pk);
+        }
+        l = l * alpha + (((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7])));
+        // O_i holds the products up to key tile j-1 (complete: S_i(j) was
+        // issued after them); rescale it to the new max before PV_i(j).
+        if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-        for (int cc = 0; cc < DH / 32; ++cc) {
-          float v[32];
-          tmem_ld32(t_o + cc * 32, v);
+          for (int cc = 0; cc < DH / 32; ++cc) {
+            float v[32];
+            tmem_ld32(t_o + cc * 32, v);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= alpha;
-          tmem_st32(t_o + cc * 32, v);
+            for (int i = 0; i < 32; ++i) v[i] *= alpha;
+            tmem_st32(t_o + cc * 32, v);
+          }
         }
+        tc_fence_before();
+        mbar_arrive(b_p);
       }
-      tc_fence_before();
-      mbar_arrive(b_p);
-    }
-    sm_ok = __all_sync(0xffffffffu, ok) && __all_sync(0xffffffffu, mbar_wait(b_pvdone + 8 * ti, 0, abort_flag));
-    sm_m = m_eff;
-    sm_l = l;
-    if (sm_ok && !args.split) {
-      {
+      sm_ok = __all_sync(0xffffffffu, ok) && __all_sync(0xffffffffu, mbar_wait(b_pvdone + 8 * ti, k & 1, abort_flag));
+      ok = sm_ok;
+      sm_m = m_eff;
+      sm_l = l;
+      if (sm_ok && !args.split) {
         tc_fence_after();
         const int grow = q0 + ti * kAttnBQ + row;
         const float inv = 1.f / l;
@@ -357,11 +397,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
           }
         }
+        // O_i has been read: the next unit's first PV_i may overwrite it
+        tc_fence_before();
+        mbar_arrive(b_ofree + 8 * ti);
       }
     }
   }
 
   if (args.split) {
+    const int unit = args.unit0 + first;   // a split launch gives each pair one unit
+    const int head = unit / args.qpairs;
+    const int q0 = (unit - head * args.qpairs) * (kAttnTilesQ * kAttnBQ);
     // Combine the pair's halves of the keys: rank r finishes query tile r.
     // Its partner sends the other tile's unnormalised O rows, running max
     // and sum into r's shared memory (the K/V ring, idle now: both CTAs'

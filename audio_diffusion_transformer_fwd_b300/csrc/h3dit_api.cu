@@ -607,6 +607,13 @@ bool attn_split_enabled() {
   return !(e && e[0] == '0');
 }
 
+// Attention's full waves on persistent CTAs (default; H3DIT_ATTN_PERSIST=0
+// one CTA per unit, an A/B switch read at every call, same bits).
+bool attn_persistent() {
+  const char* e = getenv("H3DIT_ATTN_PERSIST");
+  return !(e && e[0] == '0');
+}
+
 h3dit_status launch_attention(const h3dit_config* c, const void* q, const void* k, const void* vt, int vt_ld,
                               int n, void* o, cudaStream_t s) {
   const int dh = c->head_dim, H = c->heads;
@@ -646,14 +653,21 @@ h3dit_status launch_attention(const h3dit_config* c, const void* q, const void* 
   const int tail = (attn_split_enabled() && units > sms && rem > 0 && 2 * rem <= sms && nkv >= 2) ? rem : 0;
   const int full = static_cast<int>(units) - tail;
   TimedLaunch tl(kAttn, s);
+  // The full waves run persistent: min(units, SMs) CTAs, each walking
+  // units first, first + grid, ... so that a CTA loads its next unit's
+  // query and first key tiles while it finishes the current one.
   auto run = [&](auto kernel, size_t smem) -> h3dit_status {
     H3_TRY(set_smem(kernel, smem));
     a.unit0 = 0;
+    a.units = full;
     a.split = 0;
-    if (full > 0) H3_TRY(launch_ex(kernel, dim3(full), dim3(h3::kAttnThreads), smem, s, 1, tq, tk, tv, a));
+    if (full > 0)
+      H3_TRY(launch_ex(kernel, dim3(std::min(full, attn_persistent() ? sms : full)), dim3(h3::kAttnThreads), smem,
+                       s, 1, tq, tk, tv, a));
     tl.kernels = (full > 0 ? 1 : 0) + (tail > 0 ? 1 : 0);
     if (tail > 0) {
       a.unit0 = full;
+      a.units = tail;
       a.split = 1;
       H3_TRY(launch_ex(kernel, dim3(2 * tail), dim3(h3::kAttnThreads), smem, s, 2, tq, tk, tv, a));
     }

@@ -59,11 +59,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait until the phase of parity `parity` has completed.  Bounded: after
-// g_wait_limit_ns (or once another role of the CTA gave up and raised *abort)
-// it records the timeout and returns false so the caller can unwind.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
+// The slow part of mbar_wait, out of line so that every wait site inlines
+// only the single try-wait of the common case (this keeps the hot loops
+// small: the attention kernel no longer spills).
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort) {
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
@@ -76,6 +75,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
       return false;
     }
   }
+}
+// Wait until the phase of parity `parity` has completed.  Bounded: after
+// g_wait_limit_ns (or once another role of the CTA gave up and raised *abort)
+// it records the timeout and returns false so the caller can unwind.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, abort);
 }
 
 // Short bounded wait used only while unwinding after an abort.

@@ -174,7 +174,8 @@ h3dit_status h3dit_check_device_error(cudaStream_t stream);
  * read at every call, H3DIT_DISABLE_GATED_ADALN once per process): H3DIT_PDL=0 plain launches; H3DIT_GEMM_SINGLE_CTA=1
  * projections on single CTAs instead of CTA pairs; H3DIT_GEMM_TAIL=0 no
  * half tiles in a short last wave; H3DIT_GEMM_BAND=k raster bands of k
- * N-tiles (default 16); H3DIT_DISABLE_GATED_ADALN=1 the gated residual and
+ * N-tiles (default 16); H3DIT_ATTN_PERSIST=0 attention with one CTA per
+ * unit instead of persistent CTAs; H3DIT_DISABLE_GATED_ADALN=1 the gated residual and
  * the following AdaLN as two launches.  One switch changes rounding:
  * H3DIT_ATTN_SPLIT=0 runs the attention units of a short last wave whole,
  * instead of as CTA pairs that each take half of the keys and combine their
