@@ -368,3 +368,32 @@ def test_attention_split_tail_units(monkeypatch, heads, dh, n):
     i = np.unravel_index(np.argmax(diff), diff.shape)
     assert rel_l2(a, b) <= 2e-3 and diff.max() <= 2.0 ** -7 * float(np.max(np.abs(b))), \
         f"rel_l2 {rel_l2(a, b):.3e}, max diff {diff.max():.3e} at {i}: {a[i]} vs {b[i]}, max|o| {np.max(np.abs(b)):.3e}"
+
+
+def test_attention_persistent_units_equal_one_cta_per_unit(monkeypatch):
+    """50 heads x 1536 tokens = 300 units: the full waves (296 units) run on
+    148 persistent CTAs that walk two units each, counting every barrier
+    phase on across units; the 4 left over run key-split.  Each output is
+    the same computation as with one CTA per unit (H3DIT_ATTN_PERSIST=0),
+    bit for bit, and follows the oracle (checked on three heads)."""
+    heads, dh, n = 50, 128, 1536
+    shape = H.BlockShape(heads * dh, heads, dh, 256)
+    r = np.random.default_rng(77)
+    q = synth.to_bf16_values(r.standard_normal((heads, n, dh)).astype(np.float32) * 1.5)
+    k = synth.to_bf16_values(r.standard_normal((heads, n, dh)).astype(np.float32) * 1.5)
+    v = synth.to_bf16_values(r.standard_normal((heads, n, dh)).astype(np.float32))
+    vt = np.ascontiguousarray(v.transpose(0, 2, 1))
+    qd, kd, vd = dev_bf16(q), dev_bf16(k), dev_bf16(vt)
+    outs = []
+    for persist in ("1", "0"):
+        monkeypatch.setenv("H3DIT_ATTN_PERSIST", persist)
+        o = torch.full((n, heads * dh), float("nan"), device="cuda", dtype=torch.bfloat16)
+        H.h3dit_attention(shape, qd, kd, vd, n, n, o)
+        H.h3dit_check_device_error()
+        outs.append(o)
+    assert torch.equal(outs[0], outs[1])
+    got = host(outs[0]).reshape(n, heads, dh)
+    assert not np.isnan(got).any()
+    for h in (0, 25, 49):
+        ref = O.attention(q[h:h + 1], k[h:h + 1], v[h:h + 1])[0]
+        _close(got[:, h], ref, rel=1e-2, amax_frac=2.0 ** -6)
