@@ -50,6 +50,8 @@
 // finishes its own tile (rank r: tile r) by the usual two-part combine.
 // The library uses it for the units of a short last wave.
 #pragma once
+#include <type_traits>
+
 #include "ptx.cuh"
 
 namespace h3 {
@@ -262,30 +264,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           ok = false;
           break;
         }
-        for (int j = 0; j < nkv; ++j) {
+        // one key tile: PV of both query tiles, and (MORE) the next tile's S
+        auto step = [&](int j, auto more_tag) -> bool {
+          constexpr bool kMore = decltype(more_tag)::value;
           const int g = base + j;
           const int st = g & 1;
-          const bool more = j + 1 < nkv;
-          if (!mbar_wait(b_vfull + 8 * st, (g >> 1) & 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(b_vfull + 8 * st, (g >> 1) & 1, abort_flag)) return false;
           // tile 0: O_0 += P_0 V_j, then S_0 of the next key tile
-          if (!mbar_wait(b_pfull, g & 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(b_pfull, g & 1, abort_flag)) return false;
           tc_fence_after();
           issue_pv(0, g, j != 0);
-          if (more) {
-            if (!mbar_wait(b_kfull + 8 * ((g + 1) & 1), ((g + 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+          if constexpr (kMore) {
+            if (!mbar_wait(b_kfull + 8 * ((g + 1) & 1), ((g + 1) >> 1) & 1, abort_flag)) return false;
             tc_fence_after();
             issue_s(0, g + 1);
           }
           // tile 1
-          if (!mbar_wait(b_pfull + 8, g & 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(b_pfull + 8, g & 1, abort_flag)) return false;
           tc_fence_after();
           issue_pv(1, g, j != 0);
           tc_commit(b_vempty + 8 * st);
-          if (more) {
+          if constexpr (kMore) {
             issue_s(1, g + 1);
             tc_commit(b_kempty + 8 * ((g + 1) & 1));
           }
-        }
+          return true;
+        };
+        for (int j = 0; j + 1 < nkv && ok; ++j) ok = step(j, std::true_type{});
+        if (ok) ok = step(nkv - 1, std::false_type{});
         if (!ok) break;
         tc_commit(b_qempty);   // every S product of the unit is complete with it
         tc_commit(b_pvdone);
