@@ -402,8 +402,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) {
-      // ---------------- MMA issuer (rank 0 of the pair)
+    if (rank == 0) {
+      // ---------------- MMA issuer (rank 0 of the pair): the whole warp runs
+      // the loop converged, one elected lane issues the MMAs and commits
+      auto wait_all = [&](uint32_t bar, uint32_t par) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, par, abort_flag));
+      };
       constexpr uint32_t idesc_full = idesc_bf16_f32(2 * kPairRows, kGemmBN);
       constexpr uint32_t idesc_half = idesc_bf16_f32(2 * kPairRows, kGemmBN / 2);
       const uint32_t a_lo0 = sdesc_lo(smem_u32(sA));
@@ -415,25 +419,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int u = cluster; u < args.num_units && ok; u += clusters, ++it) {
         const uint32_t idesc = u < args.full_tiles ? idesc_full : idesc_half;
         const int acc = it & 1;
-        if (!mbar_wait(tempty0 + 8 * acc, ((it >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+        if (!wait_all(tempty0 + 8 * acc, ((it >> 1) & 1) ^ 1)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kGemmBN;
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) { ok = false; break; }
+          if (!wait_all(full0 + 8 * stage, phase)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_lo = a_lo0 + stage * (kPairABytes >> 4);
           const uint32_t b_lo = b_lo0 + stage * (kPairBBytes >> 4);
-#pragma unroll
-          for (int k = 0; k < kGemmBK / 16; ++k)
-            tc_mma_pair_lo(d_tmem, a_lo + 2 * k, b_lo + 2 * k, idesc, (kb | k) != 0);
-          tc_commit_pair(empty0 + 8 * stage, 0x3);
+          static_assert(kGemmBK == 64, "one four-MMA group per k-block");
+          tc_mma_k64_elect<true>(d_tmem, a_lo, b_lo, idesc, kb != 0);
+          tc_commit_pair_elect(empty0 + 8 * stage, 0x3);
           if (++stage == kPairStages) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
-        tc_commit_pair(tfull0 + 8 * acc, 0x3);
+        tc_commit_pair_elect(tfull0 + 8 * acc, 0x3);
       }
-      // every MMA issued by this thread has completed once `drain` flips
-      tc_commit_pair(drain, 0x1);
+      // every MMA issued by the elected lane has completed once `drain` flips
+      tc_commit_pair_elect(drain, 0x1);
       mbar_wait_drain(drain, 0);
     }
   } else {

@@ -241,8 +241,12 @@ __global__ void __launch_bounds__(kI8Threads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) {
-      // ---------------- MMA issuer: one accumulator per chunk, alternating
+    if (rank == 0) {
+      // ---------------- MMA issuer: one accumulator per chunk, alternating;
+      // the whole warp runs the loop converged, one elected lane issues
+      auto wait_all = [&](uint32_t bar, uint32_t par) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, par, abort_flag));
+      };
       constexpr uint32_t idesc_full = idesc_bf16_f32(kTileM, kGemmBN);
       constexpr uint32_t idesc_half = idesc_bf16_f32(kTileM, kGemmBN / 2);
       const uint32_t a_lo0 = sdesc_lo(smem_u32(sA));
@@ -255,33 +259,29 @@ __global__ void __launch_bounds__(kI8Threads, 1)
         const uint32_t idesc = u < args.full_tiles ? idesc_full : idesc_half;
         for (int ch = 0; ch < nchunks && ok; ++ch, ++cc) {
           const int acc = cc & 1;
-          if (!mbar_wait(tempty0 + 8 * acc, ((cc >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+          if (!wait_all(tempty0 + 8 * acc, ((cc >> 1) & 1) ^ 1)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + acc * kGemmBN;
           const int kb0 = ch * qa.chunk_kb;
           const int kb1 = min(kblocks, kb0 + qa.chunk_kb);
           for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) { ok = false; break; }
+            if (!wait_all(full0 + 8 * stage, phase)) { ok = false; break; }
             tc_fence_after();
             const uint32_t a_lo = a_lo0 + stage * (kABytes >> 4);
             const uint32_t b_lo = b_lo0 + stage * (kBBytes >> 4);
-#pragma unroll
-            for (int k = 0; k < kGemmBK / 16; ++k) {
-              const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
-              if constexpr (PAIR) tc_mma_pair_lo(d_tmem, a_lo + 2 * k, b_lo + 2 * k, idesc, accum);
-              else tc_mma_ss_lo(d_tmem, a_lo + 2 * k, b_lo + 2 * k, idesc, accum);
-            }
-            if constexpr (PAIR) tc_commit_pair(empty0 + 8 * stage, 0x3);
-            else tc_commit(empty0 + 8 * stage);
+            static_assert(kGemmBK == 64, "one four-MMA group per k-block");
+            tc_mma_k64_elect<PAIR>(d_tmem, a_lo, b_lo, idesc, kb != kb0);
+            if constexpr (PAIR) tc_commit_pair_elect(empty0 + 8 * stage, 0x3);
+            else tc_commit_elect(empty0 + 8 * stage);
             if (++stage == kStages) { stage = 0; phase ^= 1; }
           }
           if (!ok) break;
-          if constexpr (PAIR) tc_commit_pair(tfull0 + 8 * acc, 0x3);
-          else tc_commit(tfull0 + 8 * acc);
+          if constexpr (PAIR) tc_commit_pair_elect(tfull0 + 8 * acc, 0x3);
+          else tc_commit_elect(tfull0 + 8 * acc);
         }
       }
-      if constexpr (PAIR) tc_commit_pair(drain, 0x1);
-      else tc_commit(drain);
+      if constexpr (PAIR) tc_commit_pair_elect(drain, 0x1);
+      else tc_commit_elect(drain);
       mbar_wait_drain(drain, 0);
     }
   } else {

@@ -540,6 +540,64 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
       : "memory");
 }
+// Four MMAs over one 64-deep K block (K16 steps 32 bytes apart: low-word
+// step 2 for both operands), cta_group::1 or ::2, issued by the elected lane
+// of a whole converged warp (see tc_mma_ss_k128).  The first accumulates if
+// `acc` is non-zero, the other three always.
+template <bool PAIR>
+__device__ __forceinline__ void tc_mma_k64_elect(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                                 uint32_t acc) {
+  if constexpr (PAIR) {
+    asm volatile(
+        "{\n"
+        " .reg .pred p, t, e;\n"
+        " .reg .b64 da, db;\n"
+        " .reg .b32 a, b;\n"
+        " elect.sync _|e, 0xffffffff;\n"
+        " setp.ne.b32 p, %4, 0;\n"
+        " setp.eq.b32 t, %4, %4;\n"
+        " mov.b64 da, {%1, %5};\n mov.b64 db, {%2, %5};\n"
+        " @e tcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %3, p;\n"
+        " add.u32 a, %1, 2;\n add.u32 b, %2, 2;\n mov.b64 da, {a, %5};\n mov.b64 db, {b, %5};\n"
+        " @e tcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %3, t;\n"
+        " add.u32 a, %1, 4;\n add.u32 b, %2, 4;\n mov.b64 da, {a, %5};\n mov.b64 db, {b, %5};\n"
+        " @e tcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %3, t;\n"
+        " add.u32 a, %1, 6;\n add.u32 b, %2, 6;\n mov.b64 da, {a, %5};\n mov.b64 db, {b, %5};\n"
+        " @e tcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %3, t;\n"
+        "}\n" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(acc), "r"(kDescHi)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n"
+        " .reg .pred p, t, e;\n"
+        " .reg .b64 da, db;\n"
+        " .reg .b32 a, b;\n"
+        " elect.sync _|e, 0xffffffff;\n"
+        " setp.ne.b32 p, %4, 0;\n"
+        " setp.eq.b32 t, %4, %4;\n"
+        " mov.b64 da, {%1, %5};\n mov.b64 db, {%2, %5};\n"
+        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n"
+        " add.u32 a, %1, 2;\n add.u32 b, %2, 2;\n mov.b64 da, {a, %5};\n mov.b64 db, {b, %5};\n"
+        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, t;\n"
+        " add.u32 a, %1, 4;\n add.u32 b, %2, 4;\n mov.b64 da, {a, %5};\n mov.b64 db, {b, %5};\n"
+        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, t;\n"
+        " add.u32 a, %1, 6;\n add.u32 b, %2, 6;\n mov.b64 da, {a, %5};\n mov.b64 db, {b, %5};\n"
+        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, t;\n"
+        "}\n" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(acc), "r"(kDescHi)
+        : "memory");
+  }
+}
+// tcgen05.commit over the pair (multicast to the CTAs of `mask`) from a
+// whole converged warp: one elected lane commits.
+__device__ __forceinline__ void tc_commit_pair_elect(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n}\n"
+      ::"r"(bar), "h"(mask)
+      : "memory");
+}
 // Arrive on an mbarrier of any CTA of the cluster (shared::cluster address),
 // with the default (CTA-scope) release: the tensor-memory accesses it
 // orders are covered by tcgen05.fence::before_thread_sync on this side and
