@@ -555,3 +555,38 @@ def test_int8_projection_tail_halves_equal_whole_tiles(monkeypatch):
     for x, y in zip(*res):
         assert torch.equal(x, y)
         assert not torch.isnan(x.float()).any()
+
+
+@pytest.mark.parametrize("case", ["acc", "per_token", "per_token_gelu", "grouped"])
+def test_int8_pair_and_single_cta_agree_bit_for_bit(monkeypatch, case):
+    """The int8 projections on CTA pairs (the default) and on single CTAs
+    (H3DIT_GEMM_SINGLE_CTA=1, the A/B reference) add the same exact int32
+    chunk sums in the same order and scale them the same way, so every
+    epilogue gives identical outputs: the raw accumulators (which also equal
+    exact integer arithmetic), per-token dequantisation with and without
+    GELU, and FC2's per-group scaling.  Ragged M and a short last wave are
+    included."""
+    m, n, k = (300, 768, 2048) if case != "grouped" else (129, 512, 4096)
+    a = synth.host_int8((m, k), seed=m + 3, stream=8)
+    b = synth.host_int8((n, k), seed=n + 3, stream=9)
+    group = 1024 if case == "grouped" else k
+    sa = synth.host_uniform((m, k // group), seed=m, stream=10, lo=1e-3, hi=3e-2)
+    sb = synth.host_uniform((n,), seed=n, stream=11, lo=1e-4, hi=2e-3)
+    ad, bd = codes_dev(a), codes_dev(b)
+    outs = []
+    for single in ("1", "0"):
+        monkeypatch.setenv("H3DIT_GEMM_SINGLE_CTA", single)
+        if case == "acc":
+            c = torch.empty((m, n), device="cuda", dtype=torch.int32)
+            H.h3dit_linear_i8_acc(ad, bd, m, n, k, c)
+        else:
+            c = torch.full((m, n), float("nan"), device="cuda", dtype=torch.bfloat16)
+            H.h3dit_linear_i8(ad, dev_f32(sa), group, bd, dev_f32(sb), m, n, k, 1 if case == "per_token_gelu" else 0,
+                              c)
+        H.h3dit_check_device_error()
+        outs.append(c)
+    assert torch.equal(outs[0], outs[1])
+    if case == "acc":
+        assert np.array_equal(outs[1].cpu().numpy().astype(np.int64), exact_acc(a, b))
+    else:
+        assert not torch.isnan(outs[1].float()).any()
