@@ -100,6 +100,7 @@ struct HeadRows {
 // floats at the start of the row's output.
 __global__ void __launch_bounds__(256)
     head_stats_kernel(const __nv_bfloat16* __restrict__ x, const __grid_constant__ HeadRows hr, int d, float eps) {
+  grid_dep_wait();
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (gw >= hr.first_warp[hr.n_heads]) return;
@@ -203,6 +204,12 @@ __global__ void __launch_bounds__(kHeadThreads, 1) final_head_kernel(const __gri
   if (warp < 8) {
     // ---------------- in-place AdaLN of the x tiles
     float mean = 0.f, rstd = 0.f;
+    // the statistics launch writes (mean, rstd) into the output rows: wait
+    // for it (launch overlap) before reading them; these warps also write
+    // the outputs.  The other roles read only x, the weights and the
+    // modulation vectors, which that launch does not write, so the x tiles
+    // start streaming before it has finished.
+    grid_dep_wait();
     if (live) {
       const float2 st = *reinterpret_cast<const float2*>(a.out + static_cast<size_t>(grow) * a.c_out);
       mean = st.x;

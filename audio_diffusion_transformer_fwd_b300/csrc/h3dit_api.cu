@@ -1476,21 +1476,31 @@ h3dit_status h3dit_final_layer(const h3dit_config* cfg, const void* x, int n_tok
   TimedLaunch tl(kRows, stream);
   tl.kernels = 2;   // statistics, then the heads
   const long long stat_threads = (long long)hr.first_warp[n_heads] * 32;
-  h3::head_stats_kernel<<<(unsigned)((stat_threads + 255) / 256), 256, 0, stream>>>(static_cast<const bf16*>(x), hr,
-                                                                                    d, cfg->eps);
-  H3_CUDA(cudaGetLastError());
+  H3_TRY(launch_ex(h3::head_stats_kernel, dim3((unsigned)((stat_threads + 255) / 256)), dim3(256), 0, stream, 1,
+                   static_cast<const bf16*>(x), hr, d, cfg->eps));
   cudaLaunchConfig_t lc{};
   lc.gridDim = dim3(max_tiles * ksplit, n_heads);
   lc.blockDim = dim3(h3::kHeadThreads);
   lc.dynamicSmemBytes = smem;
   lc.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = ksplit;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (ksplit > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = ksplit;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  // the head kernel's x loads overlap the statistics launch's tail; its
+  // transform warps wait for that launch before reading the statistics
+  if (pdl_enabled()) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   lc.attrs = attr;
-  lc.numAttrs = ksplit > 1 ? 1 : 0;
+  lc.numAttrs = na;
   H3_CUDA(cudaLaunchKernelEx(&lc, h3::final_head_kernel, hb));
   return H3DIT_OK;
 }
