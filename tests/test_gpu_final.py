@@ -108,3 +108,57 @@ def test_final_layer_errors():
         with pytest.raises(H.H3DitError) as e:
             H.h3dit_final_layer(shape, x, n, [H.final_head(spec[0], spec[1], v, v, wt, spec[2], out)])
         assert e.value.status == status
+
+
+def test_final_layer_enqueued_behind_a_step_reads_the_step_output():
+    """Both final-layer launches may be scheduled before the kernel ahead of
+    them on the stream has finished (programmatic dependent launch): the
+    statistics launch waits for it before reading x, and the head kernel's
+    transform warps wait for the statistics before reading them.  Enqueued
+    straight behind a 4-block step, with no host synchronisation between,
+    the layer gives exactly what it gives on the step's output afterwards."""
+    w = TINY
+    n = w.n_tokens
+    shape = shape_of(w)
+    nb = 4
+    pos = dev_f32(synth.positions(w.video, w.n_text, w.n_audio))
+    x = dev_bf16(synth.host_activations(n, w.d, seed=71))
+    devs = [{k: dev_bf16(v) for k, v in synth.host_block_weights(w.d, w.ffn, seed=71, block=b).items()}
+            for b in range(nb)]
+    bws = [H.block_weights(dv["w_qkv"], dv["w_o"], dv["w1"], dv["w2"]) for dv in devs]
+    mods = dev_f32(np.stack([synth.host_mod(w.d, seed=71, block=b) for b in range(nb)]))
+    nbytes = H.h3dit_workspace_size(shape, n)
+    ws = torch.empty(nbytes, device="cuda", dtype=torch.uint8)
+    specs = [(0, 192, 64), (240, 16, 32)]
+    params = []
+    for k, (r0, rows, c) in enumerate(specs):
+        mod = synth.host_mod(w.d, seed=71, block=50 + k, std=0.3)
+        wt = synth.host_block_weights(w.d, c, seed=71, block=60 + k)["w1"]
+        params.append((r0, rows, c, dev_f32(mod[0]), dev_f32(mod[1]), dev_bf16(wt)))
+
+    def heads():
+        hs, outs = [], []
+        for r0, rows, c, sh, sc, wd in params:
+            out = torch.full((rows, c), float("nan"), device="cuda", dtype=torch.bfloat16)
+            hs.append(H.final_head(r0, rows, sh, sc, wd, c, out))
+            outs.append(out)
+        return hs, outs
+
+    heads_a, outs_a = heads()
+    heads_b, outs_b = heads()
+    torch.cuda.synchronize()
+    H.h3dit_step_forward(shape, bws, mods, x, pos, n, None, ws, nbytes)
+    H.h3dit_final_layer(shape, x, n, heads_a)
+    torch.cuda.synchronize()
+    H.h3dit_check_device_error()
+    x_after = x.clone()
+    torch.cuda.synchronize()
+    H.h3dit_final_layer(shape, x_after, n, heads_b)
+    H.h3dit_check_device_error()
+    for a, b in zip(outs_a, outs_b):
+        assert torch.equal(a, b)
+        assert not torch.isnan(a.float()).any()
+    xh = host(x_after)
+    for (r0, rows, c, sh, sc, wd), out in zip(params, outs_b):
+        ref_bf = O.final_head(xh, r0, rows, host(sh), host(sc), host(wd), w.eps, bf16_storage=True)
+        assert rel_l2(host(out), ref_bf) <= 5e-3
